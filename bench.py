@@ -1,0 +1,421 @@
+"""Benchmark of the weight-only quantized linear layer on GB300.
+
+One step = one pass of the decode sweep: bits {5,6,7} x N {5120,17408} x
+M {1,4,16}, K = 5120, group 128 (18 GEMMs, each on its own copy of the packed
+weights, so a step streams ~0.78 GB of distinct weights: inputs larger than
+L2). The value is whole-job decode throughput in GB/s of packed weight bytes.
+A prefill GEMM (M = 8192) is timed separately and reported under "prefill".
+
+    python bench.py [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs the same workload on its own GPU (replicas; the
+layer needs no exchange between GPUs); the step time is the maximum over
+ranks and the value sums the bytes of all ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode weight-stream GB/s (M≤16) and prefill TFLOPS (M≥4096), % of GB300 roofline"
+K_DIM = 5120
+DECODE_BITS = (5, 6, 7)
+DECODE_N = (5120, 17408)
+DECODE_M = (1, 4, 16)
+PREFILL = dict(M=8192, N=17408, K=5120, bits=6)
+WORKLOAD = ("decode sweep: bits {5,6,7} x N {5120,17408} x M {1,4,16}, K=5120, group=128, "
+            "x bf16 N(0,1), codes uniform, scales 0.01|N(0,1)| with random sign")
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    for f in ("gemv.cu", "wq_device.cuh"):
+        h.update(open(os.path.join(ROOT, "weight_only_int2_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_record():
+    """DRAM bytes per launch of the decode kernel from a committed ncu summary,
+    valid only while the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "decode_gemv_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_hash") != _kernel_hash():
+        return None
+    return d
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def _make_case_inputs(wq, torch, bits, N, M, seed):
+    import wq_inputs as I
+
+    codes = torch.from_numpy(I.make_codes(N, K_DIM, bits, seed)).cuda()
+    s = I.make_scales(N, K_DIM // 128, seed + 1)
+    s_dev = torch.from_numpy(s.view(np.int16)).view(torch.bfloat16).cuda()
+    packed, s_dev = wq.wna16_repack(codes, s_dev, bits)
+    del codes
+    x = I.make_x(M, K_DIM, seed + 2)
+    x_host = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    return dict(bits=bits, N=N, M=M, packed=packed, scales=s_dev, x=x_host.cuda(), x_host=x_host,
+                y=torch.empty((M, N), dtype=torch.bfloat16, device="cuda"),
+                y_host=torch.empty((M, N), dtype=torch.bfloat16).pin_memory(),
+                ws=torch.zeros(max(1, wq.wna16_workspace_bytes(M, N, K_DIM, bits)), dtype=torch.uint8,
+                               device="cuda"),
+                bytes=N * wq.packed_words_per_row(K_DIM, bits) * 4)
+
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    import weight_only_int2_gb300 as wq
+    from weight_only_int2_gb300 import _build
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    _build.build()
+    wq.load()
+
+    cases = []
+    seed = 2000
+    for bits in DECODE_BITS:
+        for N in DECODE_N:
+            for M in DECODE_M:
+                if args.case is None or args.case == (bits, N, M):
+                    cases.append(_make_case_inputs(wq, torch, bits, N, M, seed))
+                seed += 10
+    step_bytes = sum(c["bytes"] for c in cases)
+    stream = torch.cuda.Stream()
+
+    def launch(c):
+        wq.wna16_gemm(c["x"], c["packed"], c["scales"], c["N"], K_DIM, c["bits"], y=c["y"], ws=c["ws"])
+
+    # one step as a CUDA graph (the timed region replays it back to back)
+    with torch.cuda.stream(stream):
+        for c in cases:  # first call sets up kernels outside the capture
+            launch(c)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for c in cases:
+            launch(c)
+    # the same step with an event between launches, for the per-case table
+    # (event nodes add their own gaps, so these durations are upper bounds)
+    evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(cases) + 1)]
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev, stream=stream):
+        evs[0].record(stream)
+        for i, c in enumerate(cases):
+            launch(c)
+            evs[i + 1].record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+        graph_ev.replay()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        # keep the GPU under the same load (untimed) until the clock sampler
+        # has covered at least a second
+        t_load = time.perf_counter()
+        while time.perf_counter() - t_load < max(0.0, 1.0 - t0.elapsed_time(t1) * 1e-3):
+            with torch.cuda.stream(stream):
+                for _ in range(20):
+                    graph.replay()
+            torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        graph_ev.replay()
+    torch.cuda.synchronize()
+    per_launch = [[evs[i].elapsed_time(evs[i + 1])] for i in range(len(cases))]
+    ms_per_step = t0.elapsed_time(t1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms_per_step], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+
+    case_rows = []
+    for i, c in enumerate(cases):
+        us = 1000 * float(np.mean(per_launch[i]))
+        case_rows.append({"bits": c["bits"], "N": c["N"], "M": c["M"], "us": round(us, 3),
+                          "GBps": round(c["bytes"] / (us * 1e-6) / 1e9, 1)})
+
+    # ---- end to end through the public API: pinned host x in, host y out
+    e2e_ms = []
+    h2d = sum(c["x_host"].numel() * 2 for c in cases)
+    d2h = sum(c["y_host"].numel() * 2 for c in cases)
+    with torch.cuda.stream(stream):
+        for it in range(args.warmup + args.steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for c in cases:
+                c["x"].copy_(c["x_host"], non_blocking=True)
+                launch(c)
+                c["y_host"].copy_(c["y"], non_blocking=True)
+            b.record(stream)
+            stream.synchronize()
+            if it >= args.warmup:
+                e2e_ms.append(a.elapsed_time(b))
+    e2e_value = world * step_bytes / (float(np.mean(e2e_ms)) * 1e-3) / 1e9
+
+    # ---- prefill (separate timed region; reported, not the headline)
+    prefill = None
+    if not args.no_prefill:
+        prefill = _time_prefill(wq, torch, stream)
+
+    hbm, bf16, bf16_sus, src = _peaks()
+    # average launch duration = step time / launches (back-to-back graph
+    # launches; the short gaps between kernels are counted against us)
+    achieved = step_bytes / (ms_per_step * 1e-3) / 1e9
+    tr = _traffic_record()
+    traffic = None
+    if tr is not None:
+        traffic = tr.get("dram_bytes_per_launch_b6_n17408_m1")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": traffic,
+                "kernel": "gemv_kernel (decode, warp MMA + TMA weight stream)",
+                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": "N*K*bits/8 packed weight bytes",
+                "duration": "CUDA events around back-to-back graph replays of the step, divided by launches"}
+    return dict(value=value, ms_per_step=ms_per_step, cases=case_rows, e2e=dict(
+        value=round(e2e_value, 1), unit="GB/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
+        prefill=prefill, roofline=roofline, clocks=clk.summary(), launches=len(cases) * args.steps,
+        bf16_peak=(bf16, bf16_sus, src))
+
+
+def _time_prefill(wq, torch, stream):
+    import wq_inputs as I
+
+    M, N, K, bits = PREFILL["M"], PREFILL["N"], PREFILL["K"], PREFILL["bits"]
+    codes = torch.from_numpy(I.make_codes(N, K, bits, 77)).cuda()
+    s = torch.from_numpy(I.make_scales(N, K // 128, 78).view(np.int16)).view(torch.bfloat16).cuda()
+    packed, s = wq.wna16_repack(codes, s, bits)
+    del codes
+    x = torch.from_numpy(I.make_x(M, K, 79).view(np.int16)).view(torch.bfloat16).cuda()
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            wq.wna16_gemm(x, packed, s, N, K, bits, y=y)
+        stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        reps = 3
+        a.record(stream)
+        for _ in range(reps):
+            wq.wna16_gemm(x, packed, s, N, K, bits, y=y)
+        b.record(stream)
+        stream.synchronize()
+    ms = a.elapsed_time(b) / reps
+    tflops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    _, bf16, bf16_sus, src = _peaks()
+    return {"config": f"M={M} N={N} K={K} bits={bits}", "ms": round(ms, 3), "TFLOPS": round(tflops, 1),
+            "peak_TFLOPS": bf16, "frac": round(tflops / bf16, 4), "peak_source": src}
+
+
+# ----------------------------------------------------------------------------- oracle arms
+
+def _cpu_time_oracle(budget_s: float):
+    """Times the CPU oracle (as it stands) on a bounded sample of the decode
+    sweep: for each (bits, N) pair a row subset of W with all M tokens of the
+    largest M. Returns (GB/s of packed weight bytes, cores used, sample text)."""
+    import oracle as O
+    import wq_inputs as I
+
+    rows = 256
+    done_bytes = 0
+    t_wall0 = time.perf_counter()
+    t_cpu0 = time.process_time()
+    n = 0
+    for bits in DECODE_BITS:
+        for N in DECODE_N:
+            q = I.make_codes(rows, K_DIM, bits, 3000 + bits)
+            s = I.make_scales(rows, K_DIM // 128, 3001 + bits)
+            p = O.pack(q, bits)                     # input preparation, untimed below
+            x = I.make_x(16, K_DIM, 3002)
+            t0 = time.perf_counter()
+            codes = O.unpack(p, K_DIM, bits)
+            for M in DECODE_M:
+                O.wna16_ref(x[:M], codes, s, bits)
+            done_bytes += rows * O.packed_words_per_row(K_DIM, bits) * 4 * len(DECODE_M)
+            n += 1
+            if time.perf_counter() - t_wall0 > budget_s:
+                break
+        if time.perf_counter() - t_wall0 > budget_s:
+            break
+    wall = time.perf_counter() - t_wall0
+    cpu = time.process_time() - t_cpu0
+    gbs = done_bytes / wall / 1e9
+    sample = (f"{n} of 6 (bits, N) pairs, {rows} rows of W each, M in {{1,4,16}}: oracle unpack "
+              f"(per-bit loops) + float64 dequant + matmul; {done_bytes} packed bytes")
+    return gbs, max(1, round(cpu / wall)), sample
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    hbm, _, _, _ = _peaks()
+    vals = []
+    sample = ""
+    cores = 1
+    for it in range(args.warmup + args.steps):
+        gbs, cores, sample = _cpu_time_oracle(budget_s=8.0)
+        if it >= args.warmup:
+            vals.append(gbs)
+    v = float(np.mean(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "arm": "CPU oracle (numpy float64) on host cores"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--case", type=str, default=None,
+                    help="restrict the decode sweep to one case 'bits,N,M' (profiling)")
+    args = ap.parse_args()
+    if args.case is not None:
+        args.case = tuple(int(v) for v in args.case.split(","))
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    r = run_ours(args, rank, world, dist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        gbs, cores, sample = _cpu_time_oracle(budget_s=args.cpu_budget)
+        cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(r["value"], 1), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+                           "l2": "inputs larger than L2: each step reads 0.78 GB of distinct packed weights",
+                           "timing": "CUDA graph of one step, CUDA events between launches"},
+                "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
+                "gpu_launches": r["launches"], "clocks": r["clocks"], "prefill": r["prefill"],
+                "cases": r["cases"]}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * wq.h -- C ABI of the weight-only quantized linear layer library (libwq.so).
+ *
+ * The layer computes y = x . dequant(W)^T, where x holds bf16 activations
+ * [M, K] and W holds b-bit integer codes (b in 2..8) with one bf16 scale per
+ * (output row, 128-wide group along K) and the symmetric zero point 2^(b-1).
+ * It also provides the W4A8 variant (per-token int8 activations, int4 codes
+ * widened to int8, integer accumulation per group) and the dequantize-and-
+ * gather of a quantized embedding table.
+ *
+ * Sources, cited by page title and section:
+ *  [CARD]  "Qwen3.8-27B-INT6-Mixed-AutoRound" model card, section "Findings"
+ *          (dense pack-quantized layout of ceil(in_features*bits/32) words per
+ *          row; symmetric groups above four bits; the embedding gather).
+ *  [INT57] "vLLM Can Run INT5-7", sections 1 and 3 (bit widths 2..8; quantized
+ *          embed_tokens / lm_head).
+ *  [VQ]    "vLLM Quantization", section "How it works" (create, repack, run).
+ *  [W4A8]  "int8 activations (W4A8) are now a one-flag serve-time knob ...",
+ *          section "Under the hood" (per-token dynamic int8 activations, int4
+ *          weights widened losslessly to int8, negative group scales).
+ *
+ * Conventions for every call
+ *  - bf16 data is passed as raw 16-bit patterns (wq_bf16).
+ *  - Every buffer pointer is a DEVICE pointer, owned and allocated by the
+ *    caller, 16-byte aligned, row-major and contiguous. The library never
+ *    allocates or frees memory and never synchronizes, except in
+ *    wq_check_status().
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream);
+ *    all work is enqueued asynchronously on it.
+ *  - group must be 128 and K (or D) a positive multiple of 128.
+ *  - Return codes: WQ_OK, or WQ_EINVAL for bad arguments (returned
+ *    synchronously, nothing enqueued), WQ_EUNSUPPORTED for a valid but
+ *    unimplemented configuration, WQ_ECUDA when a CUDA call or a launch fails.
+ *    wq_last_error() gives a one-line reason for the last failure on the
+ *    calling thread.
+ *  - Kernels never trap. A pipeline wait that exceeds its bound records
+ *    WQ_ETIMEOUT in a per-device status word and the kernel returns early;
+ *    wq_check_status() reads and clears that word.
+ *
+ * Packed layout ("v1", identical to the compressed-tensors dense layout [CARD]):
+ *  row n of W is ceil(K*bits/32) little-endian uint32 words; code k occupies
+ *  stream bits [k*bits, k*bits + bits), where stream bit j is bit (j % 32) of
+ *  word j / 32 (least significant bit first, the bit order of the word-aligned
+ *  formula quoted in [CARD]). Because K is a multiple of 128, every
+ *  (row, group) block is exactly 16*bits bytes at a 16-byte-aligned offset.
+ *  Scales are bf16 [N, K/128].
+ */
+#ifndef WQ_H_
+#define WQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WQ_OK = 0,
+  WQ_EINVAL = 1,
+  WQ_EUNSUPPORTED = 2,
+  WQ_ECUDA = 3,
+  WQ_ETIMEOUT = 4
+} wq_status;
+
+typedef uint16_t wq_bf16; /* raw bf16 bit pattern */
+
+/* Words per packed row: ceil(K * bits / 32) [CARD]. Host-only, never fails
+ * (returns 0 for bits outside 1..32 or K < 0). */
+size_t wq_packed_words_per_row(int64_t K, int bits);
+
+/* Repack ("Repack: reorder weights into the layout the kernel wants" [VQ]).
+ *  codes      [N, K] uint8, one code per byte, expected in [0, 2^bits - 1].
+ *  scales     [N, K/128] bf16, any sign [W4A8].
+ *  packed     [N, ceil(K*bits/32)] uint32 output in the v1 layout.
+ *  scales_out [N, K/128] bf16 output (a copy; may equal `scales`).
+ *  bad_count  optional (NULL allowed) device int32; the number of codes above
+ *             2^bits - 1 is ADDED to it. Such codes are packed as their low
+ *             `bits` bits.
+ *  bits in 2..8. */
+wq_status wna16_repack(const uint8_t* codes, const wq_bf16* scales, int64_t N, int64_t K,
+                       int bits, int group, uint32_t* packed, wq_bf16* scales_out,
+                       int32_t* bad_count, void* stream);
+
+/* Bytes of workspace wna16_gemm needs for this shape (0 when none). */
+size_t wna16_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits);
+
+/* WNA16 linear layer [INT57 s.1, CARD]:
+ *   y[m, n] = sum_k x[m, k] * s[n, k/128] * (q[n, k] - 2^(bits-1)),
+ * float32 accumulation, y rounded to bf16 (round-to-nearest-even).
+ *  x        [M, K] bf16.        Wpacked [N, ceil(K*bits/32)] uint32 (v1 layout).
+ *  scales   [N, K/128] bf16.    y       [M, N] bf16 output.
+ *  workspace, ws_bytes: device scratch of at least wna16_workspace_bytes();
+ *             it must be zero-filled before its first use and every call that
+ *             returns WQ_OK leaves it zero-filled again. Calls that may run
+ *             concurrently must not share one workspace. May be NULL when the
+ *             required size is 0.
+ *  M >= 1, N >= 1, bits in 2..8. */
+wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const wq_bf16* scales,
+                     int64_t N, int64_t K, int bits, int group, wq_bf16* y,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* Per-token dynamic int8 activation quantization [W4A8], IEEE float32:
+ *   sx[m] = max_k |x[m, k]| / 127 (IEEE division),
+ *   xq[m, k] = clamp(round_half_even(x[m, k] / sx[m]), -127, 127)
+ * (IEEE division, not a reciprocal multiply); an all-zero row gives sx = 0 and
+ * xq = 0. x [M, K] bf16 -> xq [M, K] int8, sx [M] float32. Non-finite inputs
+ * give unspecified results. */
+wq_status act_quant_int8(const wq_bf16* x, int64_t M, int64_t K, int8_t* xq, float* sx,
+                         void* stream);
+
+/* Bytes of zero-at-rest workspace w4a8_gemm needs (split-K partials; 0 when
+ * none). Same contract as the workspace of wna16_gemm. */
+size_t w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Bytes of scratch w4a8_gemm needs for the quantized activations (xq [M, K]
+ * int8 and sx [M] float32). Its contents need not be zero and are left
+ * undefined. */
+size_t w4a8_scratch_bytes(int64_t M, int64_t K);
+
+/* W4A8 linear layer [W4A8]: act_quant_int8(x) into `scratch`, then with int4
+ * codes q and zero point 8,
+ *   acc[m, n, g] = sum_{k in group g} xq[m, k] * (q[n, k] - 8)   (exact, int32)
+ *   y[m, n] = bf16( sx[m] * sum_g s[n, g] * acc[m, n, g] ).
+ *  Wpacked4 [N, K/8] uint32 (v1 layout, bits = 4); scales [N, K/128] bf16.
+ *  workspace, ws_bytes: at least w4a8_workspace_bytes(); zero-fill contract
+ *             as for wna16_gemm (may be NULL when that size is 0).
+ *  scratch, scratch_bytes: at least w4a8_scratch_bytes(); must not overlap the
+ *             workspace. */
+wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const wq_bf16* scales,
+                    int64_t N, int64_t K, int group, wq_bf16* y, void* workspace,
+                    size_t ws_bytes, void* scratch, size_t scratch_bytes, void* stream);
+
+/* Quantized embedding gather [INT57 s.3, CARD "Findings" first bullet], any
+ * bits in 2..8 on the dense layout:
+ *   out[t, d] = bf16_RNE( float(s[ids[t], d/128]) * float(q[ids[t], d] - 2^(bits-1)) )
+ * (the float32 product is exact, so this is one rounding; a zero code offset
+ * times a negative scale gives -0.0).
+ *  ids [T] int32; Wpacked [V, ceil(D*bits/32)] uint32; scales [V, D/128] bf16;
+ *  out [T, D] bf16. Ids outside [0, V) produce a +0.0 row and, when bad_count
+ *  is not NULL, are added to *bad_count. T >= 0 (T = 0 enqueues nothing). */
+wq_status qembed_gather(const int32_t* ids, int64_t T, const uint32_t* Wpacked,
+                        const wq_bf16* scales, int64_t V, int64_t D, int bits, int group,
+                        wq_bf16* out, int32_t* bad_count, void* stream);
+
+/* ---- test and debug entry points ---------------------------------------- */
+
+/* Inverse of the repack for the codes: packed [N, ceil(K*bits/32)] ->
+ * codes [N, K] uint8. */
+wq_status wq_debug_unpack(const uint32_t* packed, int64_t N, int64_t K, int bits,
+                          uint8_t* codes, void* stream);
+
+/* The exact per-group integer accumulators of the W4A8 main loop [W4A8]:
+ *   acc[m, n, g] = sum_{k in group g} xq[m, k] * (q[n, k] - 8)
+ * computed by the same kernel as w4a8_gemm. xq [M, K] int8, Wpacked4 as in
+ * w4a8_gemm, acc [M, N, K/128] int32 output. */
+wq_status wq_debug_w4a8_group_acc(const int8_t* xq, int64_t M, const uint32_t* Wpacked4,
+                                  int64_t N, int64_t K, int32_t* acc, void* stream);
+
+/* Reads and clears the status word of the current device (synchronizes the
+ * device). Returns WQ_OK, WQ_ETIMEOUT if a kernel gave up on a pipeline wait,
+ * or WQ_ECUDA if the device reports an error. */
+wq_status wq_check_status(void);
+
+/* One-line description of the last error on the calling thread ("" if none). */
+const char* wq_last_error(void);
+
+/* Library version string. */
+const char* wq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQ_H_ */

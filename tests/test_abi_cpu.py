@@ -1,0 +1,87 @@
+"""CPU checks of the C ABI surface: the library loads, exports every symbol
+declared in include/wq.h, answers the host-only size queries, and rejects bad
+arguments before touching any GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wq.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    skip = {"if", "sizeof", "defined"}
+    return sorted({n for n in names if n not in skip})
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import weight_only_int2_gb300 as wq
+
+    if not os.path.exists(wq.LIB_PATH):
+        import __graft_entry__
+
+        __graft_entry__.build()
+    return wq.load()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ["wna16_repack", "wna16_gemm", "w4a8_gemm", "qembed_gather", "act_quant_int8",
+              "wq_packed_words_per_row", "wq_check_status", "wq_last_error"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_binding_covers_every_declared_symbol():
+    from weight_only_int2_gb300._lib import SIGNATURES
+
+    assert sorted(SIGNATURES) == _declared_functions()
+
+
+@pytest.mark.parametrize("bits", range(2, 9))
+@pytest.mark.parametrize("K", [128, 5120, 248320])
+def test_packed_words_match_oracle(lib, bits, K):
+    assert lib.wq_packed_words_per_row(K, bits) == O.packed_words_per_row(K, bits)
+
+
+def test_workspace_sizes(lib):
+    assert lib.wna16_workspace_bytes(1, 17408, 5120, 6) >= 17408 * 4
+    assert lib.wna16_workspace_bytes(4096, 17408, 5120, 6) == 0
+    assert lib.w4a8_workspace_bytes(8, 100, 256) >= 8 * 100 * 4
+    assert lib.w4a8_scratch_bytes(8, 256) >= 8 * 256 + 8 * 4
+
+
+def test_bad_arguments_rejected_before_any_cuda_call(lib):
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+    # bits out of range
+    assert lib.wna16_gemm(fake, 1, fake, fake, 8, 128, 9, 128, fake, None, 0, None) == 1
+    assert b"bits" in lib.wq_last_error()
+    # group other than 128
+    assert lib.wna16_gemm(fake, 1, fake, fake, 8, 128, 6, 64, fake, None, 0, None) == 2
+    # K not a multiple of 128
+    assert lib.wna16_repack(fake, fake, 4, 100, 6, 128, fake, fake, None, None) == 1
+    # null pointers and misalignment
+    assert lib.wna16_gemm(None, 1, fake, fake, 8, 128, 6, 128, fake, None, 0, None) == 1
+    assert lib.wna16_gemm(ctypes.c_void_p((1 << 20) + 2), 1, fake, fake, 8, 128, 6, 128, fake, None, 0,
+                          None) == 1
+    assert b"aligned" in lib.wq_last_error()
+    # M = 0
+    assert lib.wna16_gemm(fake, 0, fake, fake, 8, 128, 6, 128, fake, None, 0, None) == 1
+    # workspace too small for a split-K decode shape
+    assert lib.wna16_gemm(fake, 1, fake, fake, 5120, 5120, 6, 128, fake, fake, 16, None) == 1
+    assert b"workspace" in lib.wq_last_error()
+    # gather: T = 0 is a no-op that needs no GPU
+    assert lib.qembed_gather(None, 0, fake, fake, 10, 128, 8, 128, fake, None, None) == 0

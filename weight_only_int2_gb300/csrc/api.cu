@@ -1,0 +1,417 @@
+// C ABI of libwq: argument checks, per-device state, TMA descriptors and
+// dispatch to the kernels. See include/wq.h for the contract of each call.
+#include "wq.h"
+#include "wq_device.cuh"
+#include "wq_internal.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+namespace wq {
+
+// Per-device status word: kernels record a bounded-wait timeout here.
+__device__ unsigned g_status_word;
+
+namespace {
+
+thread_local char t_err[512] = "";
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  bool ready = false;
+  unsigned* status = nullptr;
+  int sm_count = 0;
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+wq_status fail(wq_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+wq_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(WQ_ECUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+// Fills `c` for the current device; sets up the device's state on first use.
+wq_status get_ctx(void* stream, Ctx* c) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(WQ_EUNSUPPORTED, "device index %d too large", dev);
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_status_word);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+      int sms = 0;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+      d.status = static_cast<unsigned*>(p);
+      d.sm_count = sms;
+      d.ready = true;
+    }
+    c->status = d.status;
+    c->sm_count = d.sm_count;
+  }
+  c->device = dev;
+  c->stream = static_cast<cudaStream_t>(stream);
+  return WQ_OK;
+}
+
+wq_status check_bits(int bits) {
+  if (bits < 2 || bits > 8) return fail(WQ_EINVAL, "bits must be in 2..8 (got %d)", bits);
+  return WQ_OK;
+}
+
+wq_status check_group_k(int group, int64_t K, const char* kname) {
+  if (group != 128) return fail(WQ_EUNSUPPORTED, "group must be 128 (got %d)", group);
+  if (K <= 0 || K % 128 != 0)
+    return fail(WQ_EINVAL, "%s must be a positive multiple of 128 (got %lld)", kname, (long long)K);
+  return WQ_OK;
+}
+
+#define WQ_TRY(expr)            \
+  do {                          \
+    wq_status _s = (expr);      \
+    if (_s != WQ_OK) return _s; \
+  } while (0)
+
+#define WQ_PTR(p)                                                         \
+  do {                                                                    \
+    if ((p) == nullptr) return fail(WQ_EINVAL, "%s is NULL", #p);          \
+    if (!aligned16(p)) return fail(WQ_EINVAL, "%s is not 16-byte aligned", #p); \
+  } while (0)
+
+}  // namespace
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+}
+
+static bool ensure_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  if (g_encode == nullptr) set_error("cuTensorMapEncodeTiled is not available from the driver");
+  return g_encode != nullptr;
+}
+
+bool make_tmap_u32_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                      uint32_t box_cols, uint32_t box_rows) {
+  if (!ensure_encode()) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 4};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled(u32 %llux%llu box %ux%u) failed: %d", (unsigned long long)cols,
+              (unsigned long long)rows, box_cols, box_rows, static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                       uint32_t box_cols, uint32_t box_rows) {
+  if (!ensure_encode()) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled(bf16 %llux%llu box %ux%u) failed: %d", (unsigned long long)cols,
+              (unsigned long long)rows, box_cols, box_rows, static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
+bool make_tmap_bf16_2d_sw128(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                             uint32_t box_cols, uint32_t box_rows) {
+  if (!ensure_encode()) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled(bf16 %llux%llu box %ux%u) failed: %d", (unsigned long long)cols,
+              (unsigned long long)rows, box_cols, box_rows, static_cast<int>(r));
+    return false;
+  }
+  return true;
+}
+
+}  // namespace wq
+
+using namespace wq;
+
+extern "C" {
+
+size_t wq_packed_words_per_row(int64_t K, int bits) {
+  if (K < 0 || bits < 1 || bits > 32) return 0;
+  return static_cast<size_t>((K * bits + 31) / 32);
+}
+
+const char* wq_last_error(void) { return t_err; }
+
+const char* wq_version(void) { return "wq 0.1 (sm_103a)"; }
+
+wq_status wna16_repack(const uint8_t* codes, const wq_bf16* scales, int64_t N, int64_t K, int bits,
+                       int group, uint32_t* packed, wq_bf16* scales_out, int32_t* bad_count,
+                       void* stream) {
+  t_err[0] = 0;
+  WQ_TRY(check_bits(bits));
+  WQ_TRY(check_group_k(group, K, "K"));
+  if (N < 1) return fail(WQ_EINVAL, "N must be >= 1");
+  WQ_PTR(codes);
+  WQ_PTR(scales);
+  WQ_PTR(packed);
+  WQ_PTR(scales_out);
+  Ctx c{};
+  WQ_TRY(get_ctx(stream, &c));
+  cudaError_t e = launch_repack(c, codes, N, K, bits, packed, bad_count);
+  if (e != cudaSuccess) return cuda_fail(e, "repack launch");
+  if (scales_out != scales) {
+    e = cudaMemcpyAsync(scales_out, scales, static_cast<size_t>(N) * (K / 128) * 2,
+                        cudaMemcpyDeviceToDevice, c.stream);
+    if (e != cudaSuccess) return cuda_fail(e, "scale copy");
+  }
+  return WQ_OK;
+}
+
+size_t wna16_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits) {
+  (void)bits;
+  if (M < 1 || N < 1 || K < 128) return 0;
+  return stream_workspace_bytes(M, N, K);
+}
+
+wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const wq_bf16* scales,
+                     int64_t N, int64_t K, int bits, int group, wq_bf16* y, void* workspace,
+                     size_t ws_bytes, void* stream) {
+  t_err[0] = 0;
+  WQ_TRY(check_bits(bits));
+  WQ_TRY(check_group_k(group, K, "K"));
+  if (M < 1 || N < 1) return fail(WQ_EINVAL, "M and N must be >= 1");
+  WQ_PTR(x);
+  WQ_PTR(Wpacked);
+  WQ_PTR(scales);
+  WQ_PTR(y);
+  const size_t need = stream_workspace_bytes(M, N, K);
+  if (need > 0) {
+    WQ_PTR(workspace);
+    if (ws_bytes < need)
+      return fail(WQ_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  }
+  Ctx c{};
+  WQ_TRY(get_ctx(stream, &c));
+  GemvArgs a{};
+  a.mode = GemvMode::kWna16;
+  a.x = x;
+  a.packed = Wpacked;
+  a.scales = scales;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bits = bits;
+  a.y = y;
+  a.ws = static_cast<float*>(workspace);
+  cudaError_t e = launch_stream_gemm(c, a);
+  if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "wna16_gemm launch");
+  return WQ_OK;
+}
+
+wq_status act_quant_int8(const wq_bf16* x, int64_t M, int64_t K, int8_t* xq, float* sx,
+                         void* stream) {
+  t_err[0] = 0;
+  if (M < 1) return fail(WQ_EINVAL, "M must be >= 1");
+  if (K <= 0 || K % 128 != 0) return fail(WQ_EINVAL, "K must be a positive multiple of 128");
+  WQ_PTR(x);
+  WQ_PTR(xq);
+  WQ_PTR(sx);
+  Ctx c{};
+  WQ_TRY(get_ctx(stream, &c));
+  cudaError_t e = launch_act_quant(c, x, M, K, xq, sx);
+  if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
+  return WQ_OK;
+}
+
+static size_t al256(size_t v) { return (v + 255) / 256 * 256; }
+
+size_t w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || N < 1 || K < 128) return 0;
+  return stream_workspace_bytes(M, N, K);
+}
+
+size_t w4a8_scratch_bytes(int64_t M, int64_t K) {
+  if (M < 1 || K < 128) return 0;
+  return al256(static_cast<size_t>(M) * K) + al256(static_cast<size_t>(M) * 4);
+}
+
+wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const wq_bf16* scales,
+                    int64_t N, int64_t K, int group, wq_bf16* y, void* workspace, size_t ws_bytes,
+                    void* scratch, size_t scratch_bytes, void* stream) {
+  t_err[0] = 0;
+  WQ_TRY(check_group_k(group, K, "K"));
+  if (M < 1 || N < 1) return fail(WQ_EINVAL, "M and N must be >= 1");
+  WQ_PTR(x);
+  WQ_PTR(Wpacked4);
+  WQ_PTR(scales);
+  WQ_PTR(y);
+  WQ_PTR(scratch);
+  const size_t need = w4a8_workspace_bytes(M, N, K);
+  if (need > 0) {
+    WQ_PTR(workspace);
+    if (ws_bytes < need) return fail(WQ_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  }
+  const size_t need_s = w4a8_scratch_bytes(M, K);
+  if (scratch_bytes < need_s)
+    return fail(WQ_EINVAL, "scratch too small: %zu < %zu bytes", scratch_bytes, need_s);
+  if (need > 0) {
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), s0 = reinterpret_cast<uintptr_t>(scratch);
+    if (w0 < s0 + need_s && s0 < w0 + need) return fail(WQ_EINVAL, "scratch overlaps the workspace");
+  }
+  Ctx c{};
+  WQ_TRY(get_ctx(stream, &c));
+  uint8_t* sb = static_cast<uint8_t*>(scratch);
+  int8_t* xq = reinterpret_cast<int8_t*>(sb);
+  float* sx = reinterpret_cast<float*>(sb + al256(static_cast<size_t>(M) * K));
+  cudaError_t e = launch_act_quant(c, x, M, K, xq, sx);
+  if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
+  GemvArgs a{};
+  a.mode = GemvMode::kW4a8;
+  a.xq = xq;
+  a.sx = sx;
+  a.packed = Wpacked4;
+  a.scales = scales;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bits = 4;
+  a.y = y;
+  a.ws = static_cast<float*>(workspace);
+  e = launch_stream_gemm(c, a);
+  if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "w4a8_gemm launch");
+  return WQ_OK;
+}
+
+wq_status qembed_gather(const int32_t* ids, int64_t T, const uint32_t* Wpacked, const wq_bf16* scales,
+                        int64_t V, int64_t D, int bits, int group, wq_bf16* out, int32_t* bad_count,
+                        void* stream) {
+  t_err[0] = 0;
+  WQ_TRY(check_bits(bits));
+  WQ_TRY(check_group_k(group, D, "D"));
+  if (T < 0 || V < 1) return fail(WQ_EINVAL, "T must be >= 0 and V >= 1");
+  if (static_cast<int64_t>(D) * bits / 8 > 200 * 1024)
+    return fail(WQ_EUNSUPPORTED, "packed row of %lld bytes exceeds shared memory", (long long)(D * bits / 8));
+  if (T == 0) return WQ_OK;
+  WQ_PTR(ids);
+  WQ_PTR(Wpacked);
+  WQ_PTR(scales);
+  WQ_PTR(out);
+  Ctx c{};
+  WQ_TRY(get_ctx(stream, &c));
+  cudaError_t e = launch_gather(c, ids, T, Wpacked, scales, V, D, bits, out, bad_count);
+  if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+  return WQ_OK;
+}
+
+wq_status wq_debug_unpack(const uint32_t* packed, int64_t N, int64_t K, int bits, uint8_t* codes,
+                          void* stream) {
+  t_err[0] = 0;
+  WQ_TRY(check_bits(bits));
+  WQ_TRY(check_group_k(128, K, "K"));
+  if (N < 1) return fail(WQ_EINVAL, "N must be >= 1");
+  WQ_PTR(packed);
+  WQ_PTR(codes);
+  Ctx c{};
+  WQ_TRY(get_ctx(stream, &c));
+  cudaError_t e = launch_unpack(c, packed, N, K, bits, codes);
+  if (e != cudaSuccess) return cuda_fail(e, "unpack launch");
+  return WQ_OK;
+}
+
+wq_status wq_debug_w4a8_group_acc(const int8_t* xq, int64_t M, const uint32_t* Wpacked4, int64_t N,
+                                  int64_t K, int32_t* acc, void* stream) {
+  t_err[0] = 0;
+  WQ_TRY(check_group_k(128, K, "K"));
+  if (M < 1 || N < 1) return fail(WQ_EINVAL, "M and N must be >= 1");
+  WQ_PTR(xq);
+  WQ_PTR(Wpacked4);
+  WQ_PTR(acc);
+  Ctx c{};
+  WQ_TRY(get_ctx(stream, &c));
+  GemvArgs a{};
+  a.mode = GemvMode::kW4a8GroupAcc;
+  a.xq = xq;
+  a.packed = Wpacked4;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bits = 4;
+  a.acc = acc;
+  cudaError_t e = launch_stream_gemm(c, a);
+  if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "group-acc launch");
+  return WQ_OK;
+}
+
+wq_status wq_check_status(void) {
+  t_err[0] = 0;
+  Ctx c{};
+  WQ_TRY(get_ctx(nullptr, &c));
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "device synchronize");
+  unsigned v = 0;
+  e = cudaMemcpy(&v, c.status, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (v != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpy(c.status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    if (v == kStatusTimeout) return fail(WQ_ETIMEOUT, "a kernel gave up on a pipeline wait");
+    return fail(WQ_ECUDA, "device status word %u", v);
+  }
+  return WQ_OK;
+}
+
+}  // extern "C"

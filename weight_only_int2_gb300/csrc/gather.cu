@@ -1,0 +1,119 @@
+// Quantized embedding gather on the dense layout, any bit width 2..8.
+//
+// "vLLM Can Run INT5-7", section 3, and the "Qwen3.8-27B-INT6-Mixed-AutoRound"
+// model card, section "Findings", first bullet: the embedding path is a
+// dequantize-and-gather of table rows, and the word-aligned kernel the card
+// describes cannot read widths that do not divide 32. This kernel reads the
+// dense ceil(D*bits/32)-word rows directly, so every width works.
+//
+// out[t, d] = bf16_RNE(float(s[id, d/128]) * float(q[id, d] - 2^(bits-1))).
+// The float32 product is exact, so the single bf16 rounding matches the
+// definition; q == zero point with a negative scale yields -0.0.
+//
+// One CTA per token: one bulk copy (TMA engine) brings the packed row into
+// shared memory, then each thread expands 32-code slices into 64 output bytes.
+#include "wq_device.cuh"
+#include "wq_internal.h"
+
+namespace wq {
+namespace {
+
+constexpr int kThreads = 128;
+
+template <int B>
+__global__ void __launch_bounds__(kThreads) gather_kernel(
+    const int32_t* __restrict__ ids, const uint32_t* __restrict__ packed,
+    const uint16_t* __restrict__ scales, int64_t V, int64_t D, uint16_t* __restrict__ out,
+    int32_t* __restrict__ bad_count, unsigned* __restrict__ status) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bar;
+  const int64_t t = blockIdx.x;
+  const int64_t id = ids[t];
+  const int64_t units = D / 32;
+  uint4* orow = reinterpret_cast<uint4*>(out + t * D);
+
+  if (id < 0 || id >= V) {
+    for (int64_t u = threadIdx.x; u < units; u += kThreads) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) orow[u * 4 + j] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (threadIdx.x == 0 && bad_count != nullptr) atomicAdd(bad_count, 1);
+    return;
+  }
+
+  const uint32_t row_bytes = static_cast<uint32_t>(units * 4 * B);
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(&bar, row_bytes);
+    bulk_load(smem, packed + id * units * B, row_bytes, &bar);
+  }
+  __syncthreads();
+  if (!mbar_wait_bounded(&bar, 0)) {
+    record_status(status, kStatusTimeout);
+    return;
+  }
+
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(smem);
+  const uint16_t* srow = scales + id * (D / 128);
+  constexpr uint32_t kMask = (1u << B) - 1u;
+  constexpr int kZero = 1 << (B - 1);
+  for (int64_t u = threadIdx.x; u < units; u += kThreads) {
+    uint32_t win[B + 1];
+#pragma unroll
+    for (int i = 0; i < B; ++i) win[i] = w[u * B + i];
+    win[B] = 0u;
+    const float s = bf16_bits_to_float(srow[u >> 2]);
+    uint32_t o[16];
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+      const int p0 = c * B, p1 = (c + 1) * B;
+      const uint32_t a = ((p0 & 31) == 0) ? win[p0 >> 5]
+                                          : __funnelshift_r(win[p0 >> 5], win[(p0 >> 5) + 1], p0 & 31);
+      const uint32_t b = ((p1 & 31) == 0) ? win[p1 >> 5]
+                                          : __funnelshift_r(win[p1 >> 5], win[(p1 >> 5) + 1], p1 & 31);
+      const float f0 = s * static_cast<float>(static_cast<int>(a & kMask) - kZero);
+      const float f1 = s * static_cast<float>(static_cast<int>(b & kMask) - kZero);
+      const __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
+      o[c >> 1] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      orow[u * 4 + j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+  }
+}
+
+template <int B>
+cudaError_t launch_b(const Ctx& c, const int32_t* ids, int64_t T, const uint32_t* packed,
+                     const uint16_t* scales, int64_t V, int64_t D, uint16_t* out,
+                     int32_t* bad_count) {
+  const size_t smem = static_cast<size_t>(D / 32) * 4 * B;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(gather_kernel<B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  gather_kernel<B><<<static_cast<unsigned>(T), kThreads, smem, c.stream>>>(
+      ids, packed, scales, V, D, out, bad_count, c.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const Ctx& c, const int32_t* ids, int64_t T, const uint32_t* packed,
+                          const uint16_t* scales, int64_t V, int64_t D, int bits, uint16_t* out,
+                          int32_t* bad_count) {
+  if (T == 0) return cudaSuccess;
+  switch (bits) {
+    case 2: return launch_b<2>(c, ids, T, packed, scales, V, D, out, bad_count);
+    case 3: return launch_b<3>(c, ids, T, packed, scales, V, D, out, bad_count);
+    case 4: return launch_b<4>(c, ids, T, packed, scales, V, D, out, bad_count);
+    case 5: return launch_b<5>(c, ids, T, packed, scales, V, D, out, bad_count);
+    case 6: return launch_b<6>(c, ids, T, packed, scales, V, D, out, bad_count);
+    case 7: return launch_b<7>(c, ids, T, packed, scales, V, D, out, bad_count);
+    case 8: return launch_b<8>(c, ids, T, packed, scales, V, D, out, bad_count);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace wq

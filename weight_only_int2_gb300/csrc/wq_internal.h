@@ -1,0 +1,90 @@
+// Host-side declarations shared by the translation units of libwq.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace wq {
+
+// Per-call launch context filled by the C-ABI layer.
+struct Ctx {
+  cudaStream_t stream;
+  unsigned* status;  // device address of this device's status word
+  int device;
+  int sm_count;
+};
+
+// Records a one-line error for wq_last_error() (thread-local).
+void set_error(const char* fmt, ...);
+
+// Builds a 2-D tiled TMA descriptor over a row-major matrix of 32-bit words.
+// Returns false (and records the reason) if the driver rejects it.
+bool make_tmap_u32_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                      uint32_t box_cols, uint32_t box_rows);
+
+// Builds a 2-D tiled TMA descriptor over a row-major bf16 matrix (no swizzle).
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                       uint32_t box_cols, uint32_t box_rows);
+
+// Builds a 2-D tiled TMA descriptor over a row-major bf16 matrix with 128-byte
+// swizzling (box inner extent of 64 elements).
+bool make_tmap_bf16_2d_sw128(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                             uint32_t box_cols, uint32_t box_rows);
+
+// ---- launchers (return cudaSuccess or the launch error) ----------------------
+
+cudaError_t launch_repack(const Ctx& c, const uint8_t* codes, int64_t N, int64_t K, int bits,
+                          uint32_t* packed, int32_t* bad_count);
+
+cudaError_t launch_unpack(const Ctx& c, const uint32_t* packed, int64_t N, int64_t K, int bits,
+                          uint8_t* codes);
+
+cudaError_t launch_act_quant(const Ctx& c, const uint16_t* x, int64_t M, int64_t K, int8_t* xq,
+                             float* sx);
+
+cudaError_t launch_gather(const Ctx& c, const int32_t* ids, int64_t T, const uint32_t* packed,
+                          const uint16_t* scales, int64_t V, int64_t D, int bits, uint16_t* out,
+                          int32_t* bad_count);
+
+// Weight-streaming GEMM (warp MMA, split-K). Modes of the same main loop.
+enum class GemvMode { kWna16 = 0, kW4a8 = 1, kW4a8GroupAcc = 2 };
+
+struct GemvArgs {
+  GemvMode mode;
+  const uint16_t* x;   // kWna16: bf16 activations [M, K]
+  const int8_t* xq;    // W4A8 modes: int8 activations [M, K]
+  const float* sx;     // kW4a8: per-token scale [M]
+  const uint32_t* packed;
+  const uint16_t* scales;
+  int64_t M, N, K;
+  int bits;
+  uint16_t* y;         // bf16 [M, N] (kWna16, kW4a8)
+  int32_t* acc;        // int32 [M, N, K/128] (kW4a8GroupAcc)
+  float* ws;           // fp32 [M, N] split-K partials (zero at rest)
+  uint32_t* counters;  // split-K arrival counters (zero at rest)
+};
+
+// Workspace bytes the weight-streaming GEMM needs for this shape.
+size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+cudaError_t launch_gemv(const Ctx& c, const GemvArgs& a);
+
+// Persistent decode kernel (M <= 16, K a multiple of 1024).
+bool decode_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count);
+size_t decode_workspace_bytes(int64_t M, int64_t N);
+cudaError_t launch_decode(const Ctx& c, const GemvArgs& a);
+
+// Routes a weight-streaming GEMM to the persistent decode kernel when it
+// applies, else to the chunked kernel.
+inline cudaError_t launch_stream_gemm(const Ctx& c, const GemvArgs& a) {
+  return decode_supported(a.M, a.N, a.K, a.bits, c.sm_count) ? launch_decode(c, a) : launch_gemv(c, a);
+}
+
+inline size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  const size_t a = gemv_workspace_bytes(M, N, K), b = decode_workspace_bytes(M, N);
+  return a > b ? a : b;
+}
+
+}  // namespace wq
