@@ -100,6 +100,27 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
                      int64_t N, int64_t K, int bits, int group, wq_bf16* y,
                      void* workspace, size_t ws_bytes, void* stream);
 
+/* WNA16 linear layer without a workspace argument, for callers that cannot
+ * allocate device memory (no counterpart on the source pages; it is a
+ * packaging of wna16_gemm). A serving engine that has reserved nearly all
+ * device memory up front for its KV-cache pool cannot supply a workspace on
+ * the request path, where a cudaMalloc may fail, stall the device or take
+ * memory promised elsewhere; a plain C caller may have no allocator at all.
+ * Same arguments and results as wna16_gemm, minus the workspace: the split-K
+ * scratch is a fixed 4 MiB __device__ array owned by the library, held by
+ * every GPU that loads it until the process exits.
+ *  - Shapes whose wna16_workspace_bytes() exceeds 4 MiB (about M*N > 1M)
+ *    return WQ_EINVAL with a message; use wna16_gemm for those.
+ *  - The scratch region used is cleared on `stream` before the GEMM, so no
+ *    state carries over between calls; calls whose executions overlap on the
+ *    GPU (other streams, other host threads) share the array and race.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+wq_status wna16_gemm_noalloc(const wq_bf16* x, int64_t M, const uint32_t* Wpacked,
+                             const wq_bf16* scales, int64_t N, int64_t K, int bits, int group,
+                             wq_bf16* y, void* stream);
+
 /* Per-token dynamic int8 activation quantization [W4A8], IEEE float32:
  *   sx[m] = max_k |x[m, k]| / 127 (IEEE division),
  *   xq[m, k] = clamp(round_half_even(x[m, k] / sx[m]), -127, 127)

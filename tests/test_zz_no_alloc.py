@@ -1,0 +1,64 @@
+"""The allocation-free entry point, wna16_gemm_noalloc, called through the C
+ABI: for callers that cannot allocate device memory (for example a serving
+engine whose memory is all reserved for its KV-cache pool), the split-K
+scratch lives in a fixed array owned by the library. Its output must match the
+regular wna16_gemm (which takes a caller workspace) within the acceptance
+tolerance, on two calls in a row, since every call shares that array.
+
+This file is collected last so that a run stopping at the first failure has
+already run every other test; it also passes on its own in a fresh process."""
+
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle as O
+import wq_inputs as I
+from helpers import assert_bf16_close, bf16_dev_to_f64, errors, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import weight_only_int2_gb300 as wq  # noqa: E402
+
+
+def _call_noalloc(lib, x, packed, s_dev, N, K, bits, y):
+    st = lib.wna16_gemm_noalloc(ctypes.c_void_p(x.data_ptr()), x.shape[0], ctypes.c_void_p(packed.data_ptr()),
+                                ctypes.c_void_p(s_dev.data_ptr()), N, K, bits, 128,
+                                ctypes.c_void_p(y.data_ptr()),
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, lib.wq_last_error().decode()
+
+
+@pytest.mark.parametrize("M,N,K,bits", [(4, 1000, 5120, 6), (1, 17408, 5120, 5), (16, 700, 2048, 7),
+                                        (3, 300, 640, 8)])
+def test_noalloc_matches_workspace_entry_point_twice(M, N, K, bits):
+    lib = wq.load()
+    x = I.make_x(M, K, 500 + M)
+    q = I.make_codes(N, K, bits, 501)
+    s = I.make_scales(N, K // 128, 502)
+    packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(s), bits)
+    xd = to_dev_bf16(x)
+    y_ref = wq.wna16_gemm(xd, packed, s_dev, N, K, bits)       # existing entry point
+    ref64 = bf16_dev_to_f64(y_ref)
+    for _ in range(2):                                         # two calls in a row
+        y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        _call_noalloc(lib, xd, packed, s_dev, N, K, bits, y)
+        torch.cuda.synchronize()
+        fro, mx = errors(bf16_dev_to_f64(y), ref64)
+        assert fro <= 5e-3 and mx <= 1e-2, (fro, mx)
+        assert_bf16_close(y, O.wna16_ref(x, q, s, bits), "noalloc vs oracle")
+    wq.check_status()
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    lib = wq.load()
+    M, N, K = 16, 248320, 5120                                  # needs ~16 MB of split-K scratch
+    fake = ctypes.c_void_p(1 << 20)
+    st = lib.wna16_gemm_noalloc(fake, M, fake, fake, N, K, 8, 128, fake, None)
+    assert st == 1
+    assert b"scratch" in lib.wq_last_error()

@@ -20,6 +20,7 @@ from ._lib import (  # noqa: F401
     w4a8_workspace_bytes,
     scratch,
     wna16_gemm,
+    wna16_gemm_noalloc,
     wna16_repack,
     wna16_workspace_bytes,
     workspace,

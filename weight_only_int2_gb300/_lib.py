@@ -31,6 +31,8 @@ SIGNATURES = {
     "wna16_workspace_bytes": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int]),
     "wna16_gemm": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_int, _c_int, _c_ptr,
                             _c_ptr, _c_size, _c_ptr]),
+    "wna16_gemm_noalloc": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_int, _c_int,
+                                    _c_ptr, _c_ptr]),
     "act_quant_int8": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr, _c_ptr]),
     "w4a8_workspace_bytes": (_c_size, [_c_i64, _c_i64, _c_i64]),
     "w4a8_scratch_bytes": (_c_size, [_c_i64, _c_i64]),
@@ -195,6 +197,22 @@ def wna16_gemm(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, N: i
     _check(load().wna16_gemm(_ptr(x), M, _ptr(packed), _ptr(scales), N, K, bits, group, _ptr(y),
                              _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _stream()),
            "wna16_gemm")
+    return y
+
+
+def wna16_gemm_noalloc(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, N: int, K: int,
+                       bits: int, group: int = 128, y: torch.Tensor | None = None):
+    """wna16_gemm without a workspace: the library's fixed scratch array is
+    used instead (for callers that cannot allocate device memory)."""
+    M = x.shape[0]
+    _need(x, "x", torch.bfloat16, (M, K))
+    _need(packed, "packed", torch.int32, (N, packed_words_per_row(K, bits)))
+    _need(scales, "scales", torch.bfloat16, (N, K // group))
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", torch.bfloat16, (M, N))
+    _check(load().wna16_gemm_noalloc(_ptr(x), M, _ptr(packed), _ptr(scales), N, K, bits, group, _ptr(y),
+                                     _stream()), "wna16_gemm_noalloc")
     return y
 
 
