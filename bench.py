@@ -50,7 +50,7 @@ def _peaks():
 
 def _kernel_hash():
     h = hashlib.sha256()
-    for f in ("gemv.cu", "wq_device.cuh"):
+    for f in ("decode.cu", "wq_unpack.cuh", "wq_device.cuh"):
         h.update(open(os.path.join(ROOT, "weight_only_int2_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -58,7 +58,7 @@ def _kernel_hash():
 def _traffic_record():
     """DRAM bytes per launch of the decode kernel from a committed ncu summary,
     valid only while the kernel source is unchanged."""
-    p = os.path.join(ROOT, "profiles", "decode_gemv_traffic.json")
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
@@ -262,10 +262,13 @@ def run_ours(args, rank, world, dist):
     tr = _traffic_record()
     traffic = None
     if tr is not None:
-        traffic = tr.get("dram_bytes_per_launch_b6_n17408_m1")
+        # DRAM bytes of one launch of the b=6, N=17408, M=1 case, scaled to
+        # the step's mean launch by packed bytes (traffic grows with them)
+        ref_bytes = 17408 * 960 * 4
+        traffic = round(tr["dram_bytes_per_launch"] * (step_bytes / len(cases)) / ref_bytes)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": traffic,
-                "kernel": "gemv_kernel (decode, warp MMA + TMA weight stream)",
+                "kernel": "decode_kernel (persistent, warp MMA + TMA weight stream)",
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": "N*K*bits/8 packed weight bytes",
                 "duration": "CUDA events around back-to-back graph replays of the step, divided by launches"}
