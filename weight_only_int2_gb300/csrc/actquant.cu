@@ -16,8 +16,11 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// kBf16Codes: write each code as a bf16 value (exact, |q| <= 127) instead of
+// int8, for the tensor-core GEMM whose operands are bf16.
+template <bool kBf16Codes>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __restrict__ x,
-                                                            int64_t K, int8_t* __restrict__ xq,
+                                                            int64_t K, void* __restrict__ xq_out,
                                                             float* __restrict__ sx) {
   const int64_t row = blockIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * K);
@@ -45,9 +48,8 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
   const float s = __fdiv_rn(m, 127.0f);
   if (threadIdx.x == 0) sx[row] = s;
 
-  uint2* qr = reinterpret_cast<uint2*>(xq + row * K);
   for (int64_t i = threadIdx.x; i < chunks; i += kThreads) {
-    uint32_t packed[2] = {0u, 0u};
+    int q[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (s > 0.0f) {
       const uint4 v = xr[i];
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -55,12 +57,23 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
       for (int j = 0; j < 8; ++j) {
         const uint32_t word = w[j >> 1];
         const float f = __uint_as_float((j & 1) ? (word & 0xFFFF0000u) : (word << 16));
-        int q = __float2int_rn(__fdiv_rn(f, s));
-        q = max(-127, min(127, q));
-        packed[j >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (j & 3));
+        q[j] = max(-127, min(127, __float2int_rn(__fdiv_rn(f, s))));
       }
     }
-    qr[i] = make_uint2(packed[0], packed[1]);
+    if constexpr (kBf16Codes) {
+      // small integers convert exactly; bf16 bits are the top half of fp32
+      uint32_t h[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        h[j] = (__float_as_uint(static_cast<float>(q[2 * j])) >> 16) |
+               (__float_as_uint(static_cast<float>(q[2 * j + 1])) & 0xFFFF0000u);
+      reinterpret_cast<uint4*>(static_cast<uint16_t*>(xq_out) + row * K)[i] = make_uint4(h[0], h[1], h[2], h[3]);
+    } else {
+      uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) packed[j >> 2] |= (static_cast<uint32_t>(q[j]) & 0xFFu) << (8 * (j & 3));
+      reinterpret_cast<uint2*>(static_cast<int8_t*>(xq_out) + row * K)[i] = make_uint2(packed[0], packed[1]);
+    }
   }
 }
 
@@ -69,7 +82,14 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
 cudaError_t launch_act_quant(const Ctx& c, const uint16_t* x, int64_t M, int64_t K, int8_t* xq,
                              float* sx) {
   if (M == 0) return cudaSuccess;
-  act_quant_kernel<<<static_cast<unsigned>(M), kThreads, 0, c.stream>>>(x, K, xq, sx);
+  act_quant_kernel<false><<<static_cast<unsigned>(M), kThreads, 0, c.stream>>>(x, K, xq, sx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_quant_bf16(const Ctx& c, const uint16_t* x, int64_t M, int64_t K, uint16_t* xqb,
+                                  float* sx) {
+  if (M == 0) return cudaSuccess;
+  act_quant_kernel<true><<<static_cast<unsigned>(M), kThreads, 0, c.stream>>>(x, K, xqb, sx);
   return cudaGetLastError();
 }
 

@@ -256,7 +256,8 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
   a.bits = bits;
   a.y = y;
   a.ws = static_cast<float*>(workspace);
-  cudaError_t e = launch_stream_gemm(c, a);
+  cudaError_t e = use_prefill(M, N, K, bits) ? launch_prefill(c, x, Wpacked, scales, M, N, K, bits, y, nullptr)
+                                             : launch_stream_gemm(c, a);
   if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "wna16_gemm launch");
   return WQ_OK;
 }
@@ -285,7 +286,8 @@ size_t w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 
 size_t w4a8_scratch_bytes(int64_t M, int64_t K) {
   if (M < 1 || K < 128) return 0;
-  return al256(static_cast<size_t>(M) * K) + al256(static_cast<size_t>(M) * 4);
+  // codes (int8, or bf16 for the tensor-core path) then the per-token scales
+  return al256(static_cast<size_t>(M) * K * 2) + al256(static_cast<size_t>(M) * 4);
 }
 
 wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const wq_bf16* scales,
@@ -315,7 +317,17 @@ wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const
   WQ_TRY(get_ctx(stream, &c));
   uint8_t* sb = static_cast<uint8_t*>(scratch);
   int8_t* xq = reinterpret_cast<int8_t*>(sb);
-  float* sx = reinterpret_cast<float*>(sb + al256(static_cast<size_t>(M) * K));
+  float* sx = reinterpret_cast<float*>(sb + al256(static_cast<size_t>(M) * K * 2));
+  if (use_prefill(M, N, K, 4)) {
+    // many tokens: codes as exact bf16 values into the tensor-core GEMM,
+    // which applies sx per output row
+    uint16_t* xqb = reinterpret_cast<uint16_t*>(sb);
+    cudaError_t e = launch_act_quant_bf16(c, x, M, K, xqb, sx);
+    if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
+    e = launch_prefill(c, xqb, Wpacked4, scales, M, N, K, 4, y, sx);
+    if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "w4a8_gemm launch");
+    return WQ_OK;
+  }
   cudaError_t e = launch_act_quant(c, x, M, K, xq, sx);
   if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
   GemvArgs a{};

@@ -44,6 +44,11 @@ cudaError_t launch_unpack(const Ctx& c, const uint32_t* packed, int64_t N, int64
 cudaError_t launch_act_quant(const Ctx& c, const uint16_t* x, int64_t M, int64_t K, int8_t* xq,
                              float* sx);
 
+// Same quantization, codes written as bf16 values (exact) for the
+// tensor-core GEMM.
+cudaError_t launch_act_quant_bf16(const Ctx& c, const uint16_t* x, int64_t M, int64_t K, uint16_t* xqb,
+                                  float* sx);
+
 cudaError_t launch_gather(const Ctx& c, const int32_t* ids, int64_t T, const uint32_t* packed,
                           const uint16_t* scales, int64_t V, int64_t D, int bits, uint16_t* out,
                           int32_t* bad_count);
@@ -76,13 +81,26 @@ bool decode_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count);
 size_t decode_workspace_bytes(int64_t M, int64_t N);
 cudaError_t launch_decode(const Ctx& c, const GemvArgs& a);
 
-// Routes a weight-streaming GEMM to the persistent decode kernel when it
-// applies, else to the chunked kernel.
+// Tensor-core GEMM for many tokens (tcgen05, dequantize-then-multiply).
+// sx, when given, multiplies output row m (the W4A8 per-token factor).
+constexpr int64_t kPrefillMinTokens = 65;
+bool prefill_supported(int64_t M, int64_t N, int64_t K, int bits);
+cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* packed, const uint16_t* scales,
+                           int64_t M, int64_t N, int64_t K, int bits, uint16_t* y, const float* sx);
+
+inline bool use_prefill(int64_t M, int64_t N, int64_t K, int bits) {
+  return M >= kPrefillMinTokens && prefill_supported(M, N, K, bits);
+}
+
+// Routes a weight-streaming GEMM (few tokens) to the persistent decode kernel
+// when it applies, else to the chunked kernel.
 inline cudaError_t launch_stream_gemm(const Ctx& c, const GemvArgs& a) {
   return decode_supported(a.M, a.N, a.K, a.bits, c.sm_count) ? launch_decode(c, a) : launch_gemv(c, a);
 }
 
+// Workspace of the path a shape takes: none for the tensor-core GEMM.
 inline size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M >= kPrefillMinTokens) return 0;
   const size_t a = gemv_workspace_bytes(M, N, K), b = decode_workspace_bytes(M, N);
   return a > b ? a : b;
 }
