@@ -40,6 +40,7 @@ PREFILL_CASES = [
     (777, 1000, 1280, 5),
     (1024, 512, 5120, 6),    # four token tiles, 40 groups
     (300, 2112, 384, 6),     # 17 row tiles, last one ragged
+    (4133, 2624, 256, 5),    # 357 tiles: several per CTA of the persistent grid
 ]
 
 

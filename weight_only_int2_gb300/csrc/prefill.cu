@@ -9,23 +9,30 @@
 // (at large batch the layer is compute bound: the weights are dequantized on
 // chip and the product runs on the tensor cores).
 //
-// One CTA computes a tile of 128 weight rows x TN tokens, D[row, token] in
-// tensor memory (MMA M = 128 rows, N = TN tokens; the weights are the A
-// operand so that a dequantized tile serves TN tokens). K advances in stages
-// of 64 (half a quantization group). Warp roles:
+// Persistent kernel, one CTA per SM. A tile is 128 weight rows x TN tokens,
+// D[row, token] in tensor memory (MMA M = 128 rows, N = TN tokens: the
+// weights are the A operand, so a dequantized tile serves TN tokens). Tiles
+// are taken in a static round-robin over the grid, weight-row tiles varying
+// fastest. K advances in stages of 64 (half a quantization group); the
+// accumulator is double-buffered in tensor memory (2 x TN columns) so that a
+// tile's epilogue overlaps the next tile's main loop. Warp roles:
 //   warp 0      TMA producer for the activation tile [TN x 64] (128-byte
 //               swizzle, zero fill past M) of each stage.
 //   warp 1      allocates tensor memory; one thread issues 4 MMAs of K = 16
-//               per stage and commits them to the stage's "empty" barrier.
+//               per stage, commits each stage to its "empty" barrier and each
+//               finished tile to its accumulator's "full" barrier.
 //   warp 2      TMA producer for the packed weights, one group [128 rows x
-//               16*b bytes] per load, into a ring of 2 slots.
-//   warps 3-10  dequantize: each thread turns one 32-code slice of one row
-//               into bf16 RN(s * (q - z)) (q - z exact, one rounding) and
-//               stores it in the K-major 128-byte-swizzled layout the MMA
-//               reads; afterwards the same 8 warps drain the accumulator
-//               (tcgen05.ld) and store bf16 outputs.
-// All mbarrier waits are bounded; a timeout records WQ_ETIMEOUT and the roles
-// stop early, the outputs of that CTA are then not written.
+//               16*b bytes] per load, into a ring of 2-4 slots.
+//   warps 3-6   epilogue: warp w drains TMEM lane quarter w % 4 (tcgen05.ld),
+//               scales by the per-token factor if any, stores bf16 outputs,
+//               then frees the accumulator buffer.
+//   warps 7-22  dequantize, in four teams of 4 warps: team j takes every
+//               fourth stage (W slot j). A thread turns the 64 codes of one
+//               weight row into bf16 RN(s * (q - z)) (q - z exact, one
+//               rounding) and stores them as one K-major 128-byte-swizzled
+//               row of the A operand.
+// All mbarrier waits are bounded; a timeout records WQ_ETIMEOUT and every
+// role stops early (outputs are then incomplete).
 #include "wq_device.cuh"
 #include "wq_internal.h"
 
@@ -34,16 +41,29 @@ namespace {
 
 constexpr int kBM = 128;  // weight rows per tile (MMA M)
 constexpr int kBK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kNS = 4;    // activation / dequantized-weight stages
-constexpr int kNP = 2;    // packed-weight slots (one group each)
-constexpr int kDeqWarps = 8;
-constexpr int kThreads = (3 + kDeqWarps) * 32;  // 352
+constexpr int kNS = 4;     // stages (activation tile + dequantized weight tile)
+constexpr int kMaxNP = 4;  // packed-weight slots, one group each (upper bound)
+constexpr int kTeamWarps = 4;                               // one team covers 128 rows x 64 codes
+constexpr int kTeams = kNS;                                 // team j fills W slot j
+constexpr int kDeqWarps = kTeams * kTeamWarps;
+constexpr int kEpiWarps = 4;                                // one per TMEM lane quarter
+constexpr int kThreads = (3 + kEpiWarps + kDeqWarps) * 32;  // 736
 constexpr int kWStageBytes = kBM * kBK * 2;     // 16 KB
 
+// Shared memory: kNS stages of (activation tile, dequantized weight tile),
+// then as many packed-weight slots (2..4) as fit.
 template <int B, int TN>
 struct Layout {
   static constexpr int kXStage = TN * kBK * 2;
   static constexpr int kPSlot = kBM * 16 * B;  // one group of 128 rows
+  static constexpr int kBudget = 227 * 1024 - 1024 - 512;  // minus alignment slack and static smem
+  static constexpr int pick_np() {
+    for (int np = kMaxNP; np >= 2; --np)
+      if (kNS * (kXStage + kWStageBytes) + np * kPSlot <= kBudget) return np;
+    return 0;
+  }
+  static constexpr int kNP = pick_np();
+  static_assert(kNP >= 2, "prefill rings do not fit shared memory");
   static constexpr int kXOff = 0;
   static constexpr int kWOff = kNS * kXStage;
   static constexpr int kPOff = kWOff + kNS * kWStageBytes;
@@ -55,6 +75,7 @@ struct PParams {
   const uint16_t* scales;  // bf16 [N, G]
   int64_t M, N, K;
   int G;
+  int row_tiles, tok_tiles;  // ceil(N / 128), ceil(M / TN)
   uint16_t* y;       // bf16 [M, N]
   const float* sx;   // per-token output factor [M] or null
   unsigned* status;
@@ -170,23 +191,39 @@ __device__ __forceinline__ void dequant_slice(const uint32_t (&w)[B], uint32_t s
   }
 }
 
+// The packed tile's shared-memory rows are 16*B bytes apart. For B = 2, 4, 8
+// that is a TMA swizzle span (32, 64, 128 B) and the tile is loaded swizzled:
+// the 16-byte chunk c of row r sits at chunk c ^ packed_xor<B>(r).
+__host__ __device__ constexpr int packed_swizzle_bytes(int b) {
+  return b == 8 ? 128 : (b == 4 ? 64 : (b == 2 ? 32 : 0));
+}
 template <int B>
-__device__ __forceinline__ void load_words(const uint8_t* src, uint32_t (&w)[B]) {
-  if constexpr (B % 4 == 0) {
+__device__ __forceinline__ int packed_xor(int r) {
+  if constexpr (B == 8) return r & 7;         // address bits 4-6 ^= 7-9
+  else if constexpr (B == 4) return (r >> 1) & 3;  // bits 4-5 ^= 7-8
+  else if constexpr (B == 2) return (r >> 2) & 1;  // bit 4 ^= bit 7
+  else return 0;
+}
+
+// N consecutive 32-bit words from shared memory, in the widest loads the
+// alignment allows (16 bytes when N % 4 == 0, else 8 when N is even).
+template <int N>
+__device__ __forceinline__ void load_words(const uint8_t* src, uint32_t (&w)[N]) {
+  if constexpr (N % 4 == 0) {
 #pragma unroll
-    for (int j = 0; j < B / 4; ++j) {
+    for (int j = 0; j < N / 4; ++j) {
       const uint4 v = reinterpret_cast<const uint4*>(src)[j];
       w[4 * j] = v.x, w[4 * j + 1] = v.y, w[4 * j + 2] = v.z, w[4 * j + 3] = v.w;
     }
-  } else if constexpr (B % 2 == 0) {
+  } else if constexpr (N % 2 == 0) {
 #pragma unroll
-    for (int j = 0; j < B / 2; ++j) {
+    for (int j = 0; j < N / 2; ++j) {
       const uint2 v = reinterpret_cast<const uint2*>(src)[j];
       w[2 * j] = v.x, w[2 * j + 1] = v.y;
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < B; ++j) w[j] = reinterpret_cast<const uint32_t*>(src)[j];
+    for (int j = 0; j < N; ++j) w[j] = reinterpret_cast<const uint32_t*>(src)[j];
   }
 }
 
@@ -196,7 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const PParams p) {
   using L = Layout<B, TN>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t xfull[kNS], wfull[kNS], empty[kNS], pfull[kNP], pempty[kNP], accb;
+  constexpr int NP = L::kNP;
+  // full[s]: the stage's activation bytes landed and its W tile is written
+  // (arrivals: the activation producer's expect-tx + the dequant team);
+  // empty[s]: the stage's MMAs completed (one commit)
+  __shared__ __align__(8) uint64_t full[kNS], empty[kNS], pfull[kMaxNP], pempty[kMaxNP];
+  __shared__ __align__(8) uint64_t tfull[2], tempty[2];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -207,28 +249,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ps = base + L::kPOff;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kBM;
-  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TN;
   const int G = p.G;
-  const int S = 2 * G;  // stages
+  const int S = 2 * G;  // stages per tile
+  // static schedule: tiles blockIdx.x, blockIdx.x + gridDim.x, ...; row
+  // tiles vary fastest so that CTAs running together share activation tiles
+  const int first = blockIdx.x, step = gridDim.x;
+  const int ntiles = p.row_tiles * p.tok_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNS; ++s) {
-      mbar_init(&xfull[s], 1);
-      mbar_init(&wfull[s], kDeqWarps);
+      mbar_init(&full[s], kTeamWarps + 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < kNP; ++s) {
+    for (int s = 0; s < NP; ++s) {
       mbar_init(&pfull[s], 1);
-      mbar_init(&pempty[s], kDeqWarps);
+      mbar_init(&pempty[s], 2 * kTeamWarps);  // the two teams of a group parity
     }
-    mbar_init(&accb, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], kEpiWarps);
+    }
     s_abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                 "r"(TN)
+                 "r"(2 * TN)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -238,129 +284,207 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == 0) {
-    // ---- activations: stage i covers k = 64 i .. 64 i + 63
+    // ---- activations: stage i of a tile covers k = 64 i .. 64 i + 63
     if (lane == 0) {
-      for (int i = 0; i < S && !s_abort; ++i) {
-        const int s = i % kNS;
-        if (i >= kNS && !mbar_wait_bounded(&empty[s], ((i / kNS) - 1) & 1)) {
-          record_status(p.status, kStatusTimeout);
-          s_abort = 1;
-          break;
+      uint32_t it = 0;  // stages issued by this CTA
+      for (int t = first; t < ntiles && !s_abort; t += step) {
+        const int m0 = (t / p.row_tiles) * TN;
+        for (int i = 0; i < S; ++i, ++it) {
+          const uint32_t s = it % kNS;
+          if (it >= kNS && !mbar_wait_bounded(&empty[s], ((it / kNS) - 1) & 1)) {
+            record_status(p.status, kStatusTimeout);
+            s_abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], L::kXStage);
+          tma_load_2d(xs + s * L::kXStage, &xmap, i * kBK, m0, &full[s]);
         }
-        mbar_arrive_expect_tx(&xfull[s], L::kXStage);
-        tma_load_2d(xs + s * L::kXStage, &xmap, i * kBK, static_cast<int>(m0), &xfull[s]);
       }
     }
+    __syncwarp();
   } else if (warp == 2) {
     // ---- packed weights: group g (128 codes of 128 rows) into slot g % 2
     if (lane == 0) {
-      for (int g = 0; g < G && !s_abort; ++g) {
-        const int sl = g % kNP;
-        if (g >= kNP && !mbar_wait_bounded(&pempty[sl], ((g / kNP) - 1) & 1)) {
-          record_status(p.status, kStatusTimeout);
-          s_abort = 1;
-          break;
+      uint32_t gi = 0;  // groups issued by this CTA
+      for (int t = first; t < ntiles && !s_abort; t += step) {
+        const int n0 = (t % p.row_tiles) * kBM;
+        for (int g = 0; g < G; ++g, ++gi) {
+          const uint32_t sl = gi % NP;
+          if (gi >= NP && !mbar_wait_bounded(&pempty[sl], ((gi / NP) - 1) & 1)) {
+            record_status(p.status, kStatusTimeout);
+            s_abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&pfull[sl], L::kPSlot);
+          tma_load_2d(ps + sl * L::kPSlot, &wmap, g * 4 * B, n0, &pfull[sl]);
         }
-        mbar_arrive_expect_tx(&pfull[sl], L::kPSlot);
-        tma_load_2d(ps + sl * L::kPSlot, &wmap, g * 4 * B, static_cast<int>(n0), &pfull[sl]);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
-    // ---- MMA issue (one thread)
+    // ---- MMA issue (one thread); accumulator buffer (tile count) % 2
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc(kBM, TN);
-      for (int i = 0; i < S; ++i) {
-        const int s = i % kNS;
-        const uint32_t par = (i / kNS) & 1;
-        if (s_abort || !mbar_wait_bounded(&wfull[s], par) || !mbar_wait_bounded(&xfull[s], par)) {
+      uint32_t it = 0, tc = 0;
+      for (int t = first; t < ntiles && !s_abort; t += step, ++tc) {
+        const uint32_t buf = tc & 1;
+        if (tc >= 2 && !mbar_wait_bounded(&tempty[buf], ((tc >> 1) - 1) & 1)) {
           record_status(p.status, kStatusTimeout);
           s_abort = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t aa = smem_u32(ws + s * kWStageBytes);
-        const uint32_t bb = smem_u32(xs + s * L::kXStage);
+        const uint32_t acc = tmem + buf * TN;
+        bool ok = true;
+        for (int i = 0; i < S; ++i, ++it) {
+          const uint32_t s = it % kNS;
+          if (s_abort || !mbar_wait_bounded(&full[s], (it / kNS) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t aa = smem_u32(ws + s * kWStageBytes);
+          const uint32_t bb = smem_u32(xs + s * L::kXStage);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          // K = 16 bf16 = 32 bytes further along the 128-byte swizzled rows
-          umma_bf16(tmem, sw128_desc(aa + 32 * kk), sw128_desc(bb + 32 * kk), idesc,
-                    (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // K = 16 bf16 = 32 bytes further along the 128-byte swizzled rows
+            umma_bf16(acc, sw128_desc(aa + 32 * kk), sw128_desc(bb + 32 * kk), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);  // fires when this stage's MMAs complete
         }
-        umma_commit(&empty[s]);
+        umma_commit(&tfull[buf]);  // fires once the tile's MMAs have completed
+        if (!ok) {
+          record_status(p.status, kStatusTimeout);
+          s_abort = 1;
+          break;
+        }
       }
-      umma_commit(&accb);  // fires once every MMA issued above has completed
     }
-  } else {
-    // ---- dequantize: thread -> (row r, 32-code half sl of the stage)
-    const int dt = threadIdx.x - 3 * 32;  // 0..255
-    const int r = dt >> 1, sl = dt & 1;
-    const int64_t row = n0 + r;
-    const bool row_ok = row < p.N;
-    const uint16_t* srow = p.scales + (row_ok ? row : 0) * static_cast<int64_t>(G);
-    uint8_t* wdst = ws + (r >> 3) * 1024 + (r & 7) * 128;
-    uint16_t sb = row_ok ? srow[0] : static_cast<uint16_t>(0);
-    for (int i = 0; i < S; ++i) {
-      const int s = i % kNS, g = i >> 1, h = i & 1, pslot = g % kNP;
-      // every decision below is warp-uniform (the warp later meets at
-      // __syncwarp and tcgen05.ld)
-      bool go = !s_abort;
-      if (go && h == 0) go = mbar_wait_bounded(&pfull[pslot], (g / kNP) & 1);
-      if (go && i >= kNS) go = mbar_wait_bounded(&empty[s], ((i / kNS) - 1) & 1);
-      if (!__all_sync(0xFFFFFFFFu, go)) {
+    __syncwarp();
+  } else if (warp < 3 + kEpiWarps) {
+    // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. weight
+    // rows n0 + 32 (w % 4) + lane, across the TN token columns
+    const int quarter = warp & 3;
+    uint32_t tc = 0;
+    for (int t = first; t < ntiles; t += step, ++tc) {
+      const uint32_t buf = tc & 1;
+      const int64_t n = static_cast<int64_t>(t % p.row_tiles) * kBM + quarter * 32 + lane;
+      const int64_t m0 = static_cast<int64_t>(t / p.row_tiles) * TN;
+      const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&tfull[buf], (tc >> 1) & 1));
+      if (!ok) {
         if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
         s_abort = 1;
         break;
       }
-      const uint32_t s2 = static_cast<uint32_t>(sb) | (static_cast<uint32_t>(sb) << 16);
-      uint32_t w[B];
-      load_words<B>(ps + pslot * L::kPSlot + r * 16 * B + (2 * h + sl) * 4 * B, w);
-      if (h == 1 && g + 1 < G && row_ok) sb = srow[g + 1];  // next group's scale
-      uint32_t o[16];
-      dequant_slice<B>(w, s2, o);
-      uint8_t* dst = wdst + s * kWStageBytes;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int c = 4 * sl + q;  // 16-byte chunk of the 128-byte row
-        *reinterpret_cast<uint4*>(dst + ((c ^ (r & 7)) << 4)) =
-            make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-      }
-      fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&wfull[s]);
-        if (h == 1) mbar_arrive(&pempty[pslot]);
-      }
-    }
-
-    // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows);
-    // the two warps of a lane quarter split the TN token columns.
-    const int quarter = warp & 3, half = (warp - 3) >> 2;
-    const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&accb, 0));
-    if (!ok && lane == 0) record_status(p.status, kStatusTimeout);
-    tc_fence_after();
-    const int64_t n = n0 + quarter * 32 + lane;
+      tc_fence_after();
+      const int mrem = static_cast<int>(p.M - m0 < TN ? p.M - m0 : TN);
+      uint16_t* dst = p.y + m0 * p.N + n;
+      const float* tok = kTok ? p.sx + m0 : nullptr;
 #pragma unroll 1
-    for (int cb = half * (TN / 2); cb < (half + 1) * (TN / 2); cb += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + cb, v);
-      if (ok && !s_abort && n < p.N) {
+      for (int cb = 0; cb < TN; cb += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * TN + cb, v);
+        if (n < p.N) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int64_t m = m0 + cb + j;
-          if (m < p.M) {
-            const float f = __uint_as_float(v[j]) * (kTok ? p.sx[m] : 1.0f);
-            p.y[m * p.N + n] = float_to_bf16_bits_rn(f);
+          for (int j = 0; j < 32; ++j) {
+            if (cb + j < mrem) {
+              const float f = __uint_as_float(v[j]) * (kTok ? tok[cb + j] : 1.0f);
+              dst[static_cast<int64_t>(cb + j) * p.N] = float_to_bf16_bits_rn(f);
+            }
           }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  } else {
+    // ---- dequantize: 4 teams of 4 warps; team j handles the stages it = j
+    // (mod 4) of the CTA's sequence (all in W slot j): groups with gi = j / 2
+    // (mod 2), half j % 2 of each. Thread -> weight row r = 32 (w % 4) + lane
+    // of the tile: 64 codes, two slices, one 128-byte swizzled W row.
+    const int dw = warp - 3 - kEpiWarps;  // 0..15
+    const int team = dw / kTeamWarps;     // == W slot
+    const int h = team & 1, gpar = team >> 1;
+    const int r = (dw % kTeamWarps) * 32 + lane;
+    uint8_t* wrow = ws + team * kWStageBytes + (r >> 3) * 1024 + (r & 7) * 128;
+    const int rsw = r & 7;
+    // the scale of the next group this thread dequantizes, loaded one use ahead
+    int nt = first, ng = gpar;
+    while (ng >= G && nt < ntiles) ng -= G, nt += step;
+    auto load_scale = [&]() -> uint16_t {
+      uint16_t v = 0;
+      if (nt < ntiles) {
+        const int64_t row = static_cast<int64_t>(nt % p.row_tiles) * kBM + r;
+        if (row < p.N) v = p.scales[row * G + ng];
+      }
+      ng += 2;
+      while (ng >= G && nt < ntiles) ng -= G, nt += step;
+      return v;
+    };
+    uint16_t sb = load_scale();
+    uint32_t gi = 0;    // groups of the CTA's sequence
+    bool stop = false;  // warp-uniform
+    for (int t = first; t < ntiles && !stop; t += step) {
+      for (int g = 0; g < G; ++g, ++gi) {
+        if (static_cast<int>(gi & 1) != gpar) continue;
+        const uint32_t it = 2 * gi + h, pslot = gi % NP;
+        // every decision below is warp-uniform (the warp meets at __syncwarp)
+        bool go = !s_abort;
+        if (go) go = mbar_wait_bounded(&pfull[pslot], (gi / NP) & 1);
+        if (go && it >= kNS) go = mbar_wait_bounded(&empty[team], ((it / kNS) - 1) & 1);
+        if (!__all_sync(0xFFFFFFFFu, go)) {
+          if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
+          s_abort = 1;
+          stop = true;
+          break;
+        }
+        const uint32_t s2 = static_cast<uint32_t>(sb) | (static_cast<uint32_t>(sb) << 16);
+        sb = load_scale();
+        uint32_t w[2 * B];
+        const uint8_t* prow = ps + pslot * L::kPSlot + r * 16 * B;
+        if constexpr (packed_swizzle_bytes(B) != 0) {
+          // half h = 16-byte chunks B/2 * h .. + B/2 - 1 of the row, swizzled
+#pragma unroll
+          for (int j = 0; j < B / 2; ++j) {
+            const int c = (B / 2) * h + j;
+            const uint4 v = *reinterpret_cast<const uint4*>(prow + ((c ^ packed_xor<B>(r)) << 4));
+            w[4 * j] = v.x, w[4 * j + 1] = v.y, w[4 * j + 2] = v.z, w[4 * j + 3] = v.w;
+          }
+        } else {
+          load_words<2 * B>(prow + h * 8 * B, w);
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t ws_[B];
+#pragma unroll
+          for (int j = 0; j < B; ++j) ws_[j] = w[half * B + j];
+          uint32_t o[16];
+          dequant_slice<B>(ws_, s2, o);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = 4 * half + q;  // 16-byte chunk of the 128-byte row
+            *reinterpret_cast<uint4*>(wrow + ((c ^ rsw) << 4)) =
+                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          }
+        }
+        fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&full[team]);
+          mbar_arrive(&pempty[pslot]);
         }
       }
     }
   }
 
+  // every warp arrives here converged (role branches end with __syncwarp or
+  // are warp-uniform), so the barrier waits for all of them
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TN) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * TN) : "memory");
   }
 }
 
@@ -376,8 +500,12 @@ cudaError_t plaunch(const Ctx& c, const CUtensorMap& xmap, const CUtensorMap& wm
     if (e != cudaSuccess) return e;
     configured[c.device] = true;
   }
-  const dim3 grid(static_cast<unsigned>((prm.N + kBM - 1) / kBM), static_cast<unsigned>((prm.M + TN - 1) / TN));
-  prefill_kernel<B, TN, kTok><<<grid, kThreads, smem, c.stream>>>(xmap, wmap, prm);
+  PParams q = prm;
+  q.row_tiles = static_cast<int>((prm.N + kBM - 1) / kBM);
+  q.tok_tiles = static_cast<int>((prm.M + TN - 1) / TN);
+  const int tiles = q.row_tiles * q.tok_tiles;
+  const int grid = tiles < c.sm_count ? tiles : c.sm_count;  // persistent: one CTA per SM
+  prefill_kernel<B, TN, kTok><<<grid, kThreads, smem, c.stream>>>(xmap, wmap, q);
   return cudaGetLastError();
 }
 
@@ -419,7 +547,9 @@ cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* pack
                                static_cast<uint32_t>(tn)))
     return cudaErrorInvalidValue;
   const uint64_t words = static_cast<uint64_t>(K) * bits / 32;
-  if (!make_tmap_u32_2d(&wmap, packed, words, static_cast<uint64_t>(N), 4u * bits, kBM))
+  // rows of a power-of-two pitch (2, 4, 8 bits: 32, 64, 128 bytes) would put
+  // every row on the same banks; the TMA swizzle of that span spreads them
+  if (!make_tmap_u32_2d(&wmap, packed, words, static_cast<uint64_t>(N), 4u * bits, kBM, packed_swizzle_bytes(bits)))
     return cudaErrorInvalidValue;
   PParams prm{};
   prm.scales = scales;

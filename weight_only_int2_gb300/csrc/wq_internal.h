@@ -20,9 +20,12 @@ struct Ctx {
 void set_error(const char* fmt, ...);
 
 // Builds a 2-D tiled TMA descriptor over a row-major matrix of 32-bit words.
-// Returns false (and records the reason) if the driver rejects it.
+// swizzle_bytes 0 (none), 32, 64 or 128: the shared-memory tile is written
+// with that TMA swizzle (16-byte chunk index XOR address bits 7 and up; the
+// destination must be aligned to the pattern). Returns false (and records the
+// reason) if the driver rejects it.
 bool make_tmap_u32_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
-                      uint32_t box_cols, uint32_t box_rows);
+                      uint32_t box_cols, uint32_t box_rows, int swizzle_bytes = 0);
 
 // Builds a 2-D tiled TMA descriptor over a row-major bf16 matrix (no swizzle).
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
