@@ -13,24 +13,26 @@
 // D[row, token] in tensor memory (MMA M = 128 rows, N = TN tokens: the
 // weights are the A operand, so a dequantized tile serves TN tokens). Tiles
 // are taken in a static round-robin over the grid, weight-row tiles varying
-// fastest. K advances in stages of 64 (half a quantization group); the
-// accumulator is double-buffered in tensor memory (2 x TN columns) so that a
-// tile's epilogue overlaps the next tile's main loop. Warp roles:
+// fastest. K advances in stages of 64 (half a quantization group).
+// Tensor memory (512 columns): the fp32 accumulator in columns 0..TN-1 and a
+// ring of 8 dequantized A stages (32 columns each) in columns 256..511, so
+// the weights never pass through shared memory once dequantized; shared
+// memory holds up to 6 activation stages and 2-4 packed-weight groups.
+// Warp roles:
 //   warp 0      TMA producer for the activation tile [TN x 64] (128-byte
 //               swizzle, zero fill past M) of each stage.
-//   warp 1      allocates tensor memory; one thread issues 4 MMAs of K = 16
-//               per stage, commits each stage to its "empty" barrier and each
-//               finished tile to its accumulator's "full" barrier.
+//   warp 1      allocates tensor memory; one thread issues, per stage, one
+//               barrier wait, 4 MMAs of K = 16 (A from tensor memory, B from
+//               shared memory) and one commit; each finished tile is
+//               committed to the accumulator's "full" barrier.
 //   warp 2      TMA producer for the packed weights, one group [128 rows x
-//               16*b bytes] per load, into a ring of 2-4 slots.
-//   warps 3-6   epilogue: warp w drains TMEM lane quarter w % 4 (tcgen05.ld),
-//               scales by the per-token factor if any, stores bf16 outputs,
-//               then frees the accumulator buffer.
-//   warps 7-22  dequantize, in four teams of 4 warps: team j takes every
-//               fourth stage (W slot j). A thread turns the 64 codes of one
-//               weight row into bf16 RN(s * (q - z)) (q - z exact, one
-//               rounding) and stores them as one K-major 128-byte-swizzled
-//               row of the A operand.
+//               16*b bytes] per load.
+//   warps 3-18  four teams of 4 warps; team j takes every fourth stage. A
+//               thread turns the 64 codes of one weight row into bf16
+//               RN(s * (q - z)) (q - z exact, one rounding) and writes them
+//               to its TMEM lane (tcgen05.st). The same warps read the
+//               accumulator out after each tile (tcgen05.ld), release it,
+//               and store bf16 outputs scaled by the per-token factor if any.
 // All mbarrier waits are bounded; a timeout records WQ_ETIMEOUT and every
 // role stops early (outputs are then incomplete).
 #include "wq_device.cuh"
@@ -39,34 +41,43 @@
 namespace wq {
 namespace {
 
-constexpr int kBM = 128;  // weight rows per tile (MMA M)
-constexpr int kBK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kNS = 4;     // stages (activation tile + dequantized weight tile)
-constexpr int kMaxNP = 4;  // packed-weight slots, one group each (upper bound)
-constexpr int kTeamWarps = 4;                               // one team covers 128 rows x 64 codes
-constexpr int kTeams = kNS;                                 // team j fills W slot j
+constexpr int kBM = 128;     // weight rows per tile (MMA M)
+constexpr int kBK = 64;      // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kNA = 8;       // A stages in tensor memory
+constexpr int kACol = 256;   // A ring: TMEM columns [256, 512), 32 per stage
+constexpr int kTmemCols = 512;
+constexpr int kMaxNX = 6;    // activation stages in shared memory (upper bound)
+constexpr int kMaxNP = 4;    // packed-weight slots, one group each (upper bound)
+constexpr int kTeamWarps = 4;                  // one team: 128 rows x 64 codes
+constexpr int kTeams = 4;                      // team j takes stages j (mod 4)
 constexpr int kDeqWarps = kTeams * kTeamWarps;
-constexpr int kEpiWarps = 4;                                // one per TMEM lane quarter
-constexpr int kThreads = (3 + kEpiWarps + kDeqWarps) * 32;  // 736
-constexpr int kWStageBytes = kBM * kBK * 2;     // 16 KB
+constexpr int kThreads = (3 + kDeqWarps) * 32;  // 608
+static_assert(kNA % kTeams == 0, "each team must own whole A slots");
 
-// Shared memory: kNS stages of (activation tile, dequantized weight tile),
-// then as many packed-weight slots (2..4) as fit.
+// Shared memory: activation stages (3..6) and packed-weight slots (2 or 4).
+// Preference: 4 packed slots with at least 5 activation stages, else the
+// deepest activation ring with 2 slots. The slot count is even: a slot's
+// previous group then has the same parity, so the teams that wait on it have
+// consumed that previous phase (a parity wait is only sound when the phase
+// before the awaited one has completed).
 template <int B, int TN>
 struct Layout {
   static constexpr int kXStage = TN * kBK * 2;
   static constexpr int kPSlot = kBM * 16 * B;  // one group of 128 rows
   static constexpr int kBudget = 227 * 1024 - 1024 - 512;  // minus alignment slack and static smem
-  static constexpr int pick_np() {
-    for (int np = kMaxNP; np >= 2; --np)
-      if (kNS * (kXStage + kWStageBytes) + np * kPSlot <= kBudget) return np;
+  static constexpr bool fits(int nx, int np) { return nx * kXStage + np * kPSlot <= kBudget; }
+  static constexpr int pick_nx() {
+    for (int nx = kMaxNX; nx >= 5; --nx)
+      if (fits(nx, kMaxNP)) return nx;
+    for (int nx = kMaxNX; nx >= 3; --nx)
+      if (fits(nx, 2)) return nx;
     return 0;
   }
-  static constexpr int kNP = pick_np();
-  static_assert(kNP >= 2, "prefill rings do not fit shared memory");
+  static constexpr int kNX = pick_nx();
+  static constexpr int kNP = fits(kNX, kMaxNP) ? kMaxNP : 2;
+  static_assert(kNX >= 3 && fits(kNX, kNP), "prefill rings do not fit shared memory");
   static constexpr int kXOff = 0;
-  static constexpr int kWOff = kNS * kXStage;
-  static constexpr int kPOff = kWOff + kNS * kWStageBytes;
+  static constexpr int kPOff = kNX * kXStage;
   static constexpr int kBytes = kPOff + kNP * kPSlot;
   static constexpr size_t kSmem = static_cast<size_t>(kBytes) + 1024;  // + alignment slack
 };
@@ -105,16 +116,6 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
@@ -137,6 +138,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// MMA with the A operand in tensor memory: A row m is TMEM lane m, and 32-bit
+// column j of the operand holds the bf16 pair (k = 2j, 2j + 1); one K = 16
+// step reads 8 columns starting at a_tmem.
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Thread t of the warp writes 32 consecutive 32-bit columns of TMEM lane
+// (base lane + t); completes with tcgen05.wait::st.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
 }
 
 // ---- dequantization --------------------------------------------------------
@@ -232,20 +260,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                    const PParams p) {
   using L = Layout<B, TN>;
+  constexpr int NX = L::kNX, NP = L::kNP;
   extern __shared__ uint8_t smem_raw[];
-  constexpr int NP = L::kNP;
-  // full[s]: the stage's activation bytes landed and its W tile is written
-  // (arrivals: the activation producer's expect-tx + the dequant team);
-  // empty[s]: the stage's MMAs completed (one commit)
-  __shared__ __align__(8) uint64_t full[kNS], empty[kNS], pfull[kMaxNP], pempty[kMaxNP];
-  __shared__ __align__(8) uint64_t tfull[2], tempty[2];
+  // full[j]: stage (j mod kNA) has its activation bytes and its A tile
+  //          (arrivals: the activation producer's expect-tx + one team);
+  // done[j]: that stage's MMAs completed (one commit), which frees its A slot
+  //          and, kNX stages later in the sequence, its activation slot;
+  // pfull/pempty: packed-weight slots; tfull/tempty: the accumulator.
+  __shared__ __align__(8) uint64_t full[kNA], done[kNA], pfull[kMaxNP], pempty[kMaxNP], tfull, tempty;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t* xs = base + L::kXOff;
-  uint8_t* ws = base + L::kWOff;
   uint8_t* ps = base + L::kPOff;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -257,24 +285,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = p.row_tiles * p.tok_tiles;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNS; ++s) {
+    for (int s = 0; s < kNA; ++s) {
       mbar_init(&full[s], kTeamWarps + 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&done[s], 1);
     }
     for (int s = 0; s < NP; ++s) {
       mbar_init(&pfull[s], 1);
-      mbar_init(&pempty[s], 2 * kTeamWarps);  // the two teams of a group parity
+      mbar_init(&pempty[s], 2 * kTeamWarps);  // the two teams that share a group
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&tfull[s], 1);
-      mbar_init(&tempty[s], kEpiWarps);
-    }
+    mbar_init(&tfull, 1);
+    mbar_init(&tempty, kDeqWarps);
     s_abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
-                 "r"(2 * TN)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -284,33 +310,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = s_tmem;
 
   if (warp == 0) {
-    // ---- activations: stage i of a tile covers k = 64 i .. 64 i + 63
+    // ---- activations: stage i of a tile covers k = 64 i .. 64 i + 63; slot
+    // it % NX is free once stage it - NX is done
     if (lane == 0) {
-      uint32_t it = 0;  // stages issued by this CTA
+      uint32_t it = 0;  // stages of this CTA's sequence
       for (int t = first; t < ntiles && !s_abort; t += step) {
         const int m0 = (t / p.row_tiles) * TN;
         for (int i = 0; i < S; ++i, ++it) {
-          const uint32_t s = it % kNS;
-          if (it >= kNS && !mbar_wait_bounded(&empty[s], ((it / kNS) - 1) & 1)) {
-            record_status(p.status, kStatusTimeout);
-            s_abort = 1;
-            break;
+          if (it >= static_cast<uint32_t>(NX)) {
+            const uint32_t j = it - NX;
+            if (!mbar_wait_bounded(&done[j % kNA], (j / kNA) & 1)) {
+              record_status(p.status, kStatusTimeout);
+              s_abort = 1;
+              break;
+            }
           }
-          mbar_arrive_expect_tx(&full[s], L::kXStage);
-          tma_load_2d(xs + s * L::kXStage, &xmap, i * kBK, m0, &full[s]);
+          uint64_t* fb = &full[it % kNA];
+          mbar_arrive_expect_tx(fb, L::kXStage);
+          tma_load_2d(xs + (it % NX) * L::kXStage, &xmap, i * kBK, m0, fb);
         }
       }
     }
     __syncwarp();
   } else if (warp == 2) {
-    // ---- packed weights: group g (128 codes of 128 rows) into slot g % 2
+    // ---- packed weights: group g (128 codes of 128 rows) into slot g % NP
     if (lane == 0) {
-      uint32_t gi = 0;  // groups issued by this CTA
+      uint32_t gi = 0;  // groups of this CTA's sequence
       for (int t = first; t < ntiles && !s_abort; t += step) {
         const int n0 = (t % p.row_tiles) * kBM;
         for (int g = 0; g < G; ++g, ++gi) {
           const uint32_t sl = gi % NP;
-          if (gi >= NP && !mbar_wait_bounded(&pempty[sl], ((gi / NP) - 1) & 1)) {
+          if (gi >= static_cast<uint32_t>(NP) && !mbar_wait_bounded(&pempty[sl], ((gi / NP) - 1) & 1)) {
             record_status(p.status, kStatusTimeout);
             s_abort = 1;
             break;
@@ -322,37 +352,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---- MMA issue (one thread); accumulator buffer (tile count) % 2
+    // ---- MMA issue (one thread): per stage one wait, 4 MMAs, one commit
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc(kBM, TN);
       uint32_t it = 0, tc = 0;
       for (int t = first; t < ntiles && !s_abort; t += step, ++tc) {
-        const uint32_t buf = tc & 1;
-        if (tc >= 2 && !mbar_wait_bounded(&tempty[buf], ((tc >> 1) - 1) & 1)) {
+        // the first MMA of a tile overwrites the accumulator: the previous
+        // tile must have been drained
+        if (tc >= 1 && !mbar_wait_bounded(&tempty, (tc - 1) & 1)) {
           record_status(p.status, kStatusTimeout);
           s_abort = 1;
           break;
         }
-        tc_fence_after();
-        const uint32_t acc = tmem + buf * TN;
         bool ok = true;
         for (int i = 0; i < S; ++i, ++it) {
-          const uint32_t s = it % kNS;
-          if (s_abort || !mbar_wait_bounded(&full[s], (it / kNS) & 1)) {
+          const uint32_t a = it % kNA;
+          if (s_abort || !mbar_wait_bounded(&full[a], (it / kNA) & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t aa = smem_u32(ws + s * kWStageBytes);
-          const uint32_t bb = smem_u32(xs + s * L::kXStage);
+          const uint32_t bb = smem_u32(xs + (it % NX) * L::kXStage);
+          const uint32_t aa = tmem + kACol + a * (kBK / 2);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            // K = 16 bf16 = 32 bytes further along the 128-byte swizzled rows
-            umma_bf16(acc, sw128_desc(aa + 32 * kk), sw128_desc(bb + 32 * kk), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            // K = 16: 8 more A columns, 32 more bytes along the swizzled B rows
+            umma_bf16_ta(tmem, aa + 8 * kk, sw128_desc(bb + 32 * kk), idesc, (i > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(&empty[s]);  // fires when this stage's MMAs complete
+          umma_commit(&done[a]);  // fires when this stage's MMAs complete
         }
-        umma_commit(&tfull[buf]);  // fires once the tile's MMAs have completed
+        umma_commit(&tfull);  // fires once the tile's MMAs have completed
         if (!ok) {
           record_status(p.status, kStatusTimeout);
           s_abort = 1;
@@ -361,54 +390,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 3 + kEpiWarps) {
-    // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. weight
-    // rows n0 + 32 (w % 4) + lane, across the TN token columns
-    const int quarter = warp & 3;
-    uint32_t tc = 0;
-    for (int t = first; t < ntiles; t += step, ++tc) {
-      const uint32_t buf = tc & 1;
-      const int64_t n = static_cast<int64_t>(t % p.row_tiles) * kBM + quarter * 32 + lane;
-      const int64_t m0 = static_cast<int64_t>(t / p.row_tiles) * TN;
-      const bool ok = __all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&tfull[buf], (tc >> 1) & 1));
-      if (!ok) {
-        if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
-        s_abort = 1;
-        break;
-      }
-      tc_fence_after();
-      const int mrem = static_cast<int>(p.M - m0 < TN ? p.M - m0 : TN);
-      uint16_t* dst = p.y + m0 * p.N + n;
-      const float* tok = kTok ? p.sx + m0 : nullptr;
-#pragma unroll 1
-      for (int cb = 0; cb < TN; cb += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * TN + cb, v);
-        if (n < p.N) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (cb + j < mrem) {
-              const float f = __uint_as_float(v[j]) * (kTok ? tok[cb + j] : 1.0f);
-              dst[static_cast<int64_t>(cb + j) * p.N] = float_to_bf16_bits_rn(f);
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
-    }
   } else {
-    // ---- dequantize: 4 teams of 4 warps; team j handles the stages it = j
-    // (mod 4) of the CTA's sequence (all in W slot j): groups with gi = j / 2
-    // (mod 2), half j % 2 of each. Thread -> weight row r = 32 (w % 4) + lane
-    // of the tile: 64 codes, two slices, one 128-byte swizzled W row.
-    const int dw = warp - 3 - kEpiWarps;  // 0..15
-    const int team = dw / kTeamWarps;     // == W slot
+    // ---- dequantize + drain (warps 3..18). Warp w owns TMEM lane quarter
+    // q = w % 4: A rows / accumulator rows 32 q .. 32 q + 31 of the tile.
+    // Team j = (w - 3) / 4 takes the stages it = j (mod 4) of the CTA's
+    // sequence: groups gi = j / 2 (mod 2), half j % 2 of each group; its
+    // thread dequantizes the 64 codes of row r = 32 q + lane into A slot
+    // it % kNA. The same warps read the accumulator out: warp (j, q) takes
+    // token columns j * TN / 4 .. + TN / 4 - 1 of rows 32 q ...
+    const int dw = warp - 3;
+    const int team = dw / kTeamWarps;
+    const int q = warp & 3;
     const int h = team & 1, gpar = team >> 1;
-    const int r = (dw % kTeamWarps) * 32 + lane;
-    uint8_t* wrow = ws + team * kWStageBytes + (r >> 3) * 1024 + (r & 7) * 128;
-    const int rsw = r & 7;
+    const int r = 32 * q + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     // the scale of the next group this thread dequantizes, loaded one use ahead
     int nt = first, ng = gpar;
     while (ng >= G && nt < ntiles) ng -= G, nt += step;
@@ -422,17 +417,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ng >= G && nt < ntiles) ng -= G, nt += step;
       return v;
     };
+    // read this warp's share of tile t's accumulator (k-th tile of the CTA),
+    // release the accumulator, then store; warp-uniform, false on timeout
+    auto drain = [&](int k, int t) -> bool {
+      constexpr int kCols = TN / kTeams;
+      if (!__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&tfull, k & 1))) {
+        if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
+        s_abort = 1;
+        return false;
+      }
+      tc_fence_after();
+      uint32_t v[kCols / 32][32];
+#pragma unroll
+      for (int c = 0; c < kCols / 32; ++c) tmem_ld32(tmem + lane_base + team * kCols + 32 * c, v[c]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty);
+      const int64_t n = static_cast<int64_t>(t % p.row_tiles) * kBM + r;
+      const int64_t m0 = static_cast<int64_t>(t / p.row_tiles) * TN + team * kCols;
+      if (n < p.N) {
+        uint16_t* dst = p.y + m0 * p.N + n;
+#pragma unroll
+        for (int c = 0; c < kCols / 32; ++c) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t m = m0 + 32 * c + j;
+            if (m < p.M) {
+              const float f = __uint_as_float(v[c][j]) * (kTok ? p.sx[m] : 1.0f);
+              dst[static_cast<int64_t>(32 * c + j) * p.N] = float_to_bf16_bits_rn(f);
+            }
+          }
+        }
+      }
+      return true;
+    };
+
     uint16_t sb = load_scale();
     uint32_t gi = 0;    // groups of the CTA's sequence
+    int pend_k = -1, pend_t = 0;  // tile whose accumulator this warp has not read yet
     bool stop = false;  // warp-uniform
-    for (int t = first; t < ntiles && !stop; t += step) {
+    int k = 0;
+    for (int t = first; t < ntiles && !stop; t += step, ++k) {
+      const uint32_t it0 = static_cast<uint32_t>(k) * static_cast<uint32_t>(S);  // the tile's first stage
       for (int g = 0; g < G; ++g, ++gi) {
         if (static_cast<int>(gi & 1) != gpar) continue;
-        const uint32_t it = 2 * gi + h, pslot = gi % NP;
-        // every decision below is warp-uniform (the warp meets at __syncwarp)
+        const uint32_t it = 2 * gi + h, a = it % kNA, pslot = gi % NP;
+        // stage it - kNA in this tile needs this tile's MMAs, which need the
+        // previous tile's accumulator drained: drain it first
+        if (pend_k >= 0 && it >= static_cast<uint32_t>(kNA) && it - kNA >= it0) {
+          if (!drain(pend_k, pend_t)) {
+            stop = true;
+            break;
+          }
+          pend_k = -1;
+        }
+        // every decision below is warp-uniform (the warp meets at __syncwarp
+        // and the .sync.aligned tcgen05 instructions)
         bool go = !s_abort;
         if (go) go = mbar_wait_bounded(&pfull[pslot], (gi / NP) & 1);
-        if (go && it >= kNS) go = mbar_wait_bounded(&empty[team], ((it / kNS) - 1) & 1);
+        if (go && it >= static_cast<uint32_t>(kNA)) go = mbar_wait_bounded(&done[a], ((it / kNA) - 1) & 1);
         if (!__all_sync(0xFFFFFFFFu, go)) {
           if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
           s_abort = 1;
@@ -454,28 +497,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           load_words<2 * B>(prow + h * 8 * B, w);
         }
+        uint32_t o[32];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          uint32_t ws_[B];
+          uint32_t wsl[B], os[16];
 #pragma unroll
-          for (int j = 0; j < B; ++j) ws_[j] = w[half * B + j];
-          uint32_t o[16];
-          dequant_slice<B>(ws_, s2, o);
+          for (int j = 0; j < B; ++j) wsl[j] = w[half * B + j];
+          dequant_slice<B>(wsl, s2, os);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int c = 4 * half + q;  // 16-byte chunk of the 128-byte row
-            *reinterpret_cast<uint4*>(wrow + ((c ^ rsw) << 4)) =
-                make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-          }
+          for (int j = 0; j < 16; ++j) o[16 * half + j] = os[j];
         }
-        fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
+        tmem_st32(tmem + lane_base + kACol + a * (kBK / 2), o);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();  // the A tile before the arrival the MMA waits on
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&full[team]);
+          mbar_arrive(&full[a]);
           mbar_arrive(&pempty[pslot]);
         }
       }
+      if (stop) break;
+      // at most one tile pending: drain the previous one before moving on
+      if (pend_k >= 0 && !drain(pend_k, pend_t)) break;
+      pend_k = k;
+      pend_t = t;
     }
+    if (!stop && pend_k >= 0) drain(pend_k, pend_t);
   }
 
   // every warp arrives here converged (role branches end with __syncwarp or
@@ -484,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * TN) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
 }
 
