@@ -57,7 +57,10 @@ def test_noalloc_matches_workspace_entry_point_twice(M, N, K, bits):
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib = wq.load()
-    M, N, K = 16, 248320, 5120                                  # needs ~16 MB of split-K scratch
+    M, N, K = 16, 248320, 2560                                  # split-K shape: ~16 MB of scratch
+    # The pointers below are fake: the call must be rejected before any launch,
+    # so first make sure this shape really needs more than the 4 MiB array.
+    assert lib.wna16_workspace_bytes(M, N, K, 8) > (4 << 20)
     fake = ctypes.c_void_p(1 << 20)
     st = lib.wna16_gemm_noalloc(fake, M, fake, fake, N, K, 8, 128, fake, None)
     assert st == 1

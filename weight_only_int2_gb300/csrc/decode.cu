@@ -177,6 +177,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     ++issued;
     if (++ig == igc) take_unit();
   };
+  // The weight prologue goes out once this warp's activation loads are in
+  // flight (so they are not queued behind it) and fills the ring while the
+  // fragments below are built.
+  if (lane == 0) {
+    take_unit();
+    for (int s = 0; s < NS && more; ++s) issue_next(s);
+  }
   // ---- activation staging, part 2: fragments, corrections
 #pragma unroll
   for (int q = 0; q < kMaxXJobs; ++q) {
@@ -197,13 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         scl[idx] = sb;
       }
     }
-  }
-  // The weight prologue starts only now: issued earlier, its stages would
-  // queue the small activation loads behind ~150 KB per SM of weight traffic
-  // and then sit idle until staging ends.
-  if (lane == 0) {
-    take_unit();
-    for (int s = 0; s < NS && more; ++s) issue_next(s);
   }
   __syncthreads();
 

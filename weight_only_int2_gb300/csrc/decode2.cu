@@ -1,0 +1,595 @@
+// Decode GEMM for M <= 16 tokens, streamed by CTA pairs: y = x . dequant(W)^T
+// at close to HBM bandwidth with no split-K workspace and no grid barrier.
+//
+// Method: "vLLM Can Run INT5-7", section 1 (WNA16 for widths 2..8); model card
+// "Qwen3.8-27B-INT6-Mixed-AutoRound", section "Findings" (dense LSB-first
+// layout, symmetric 2^(b-1) zero point, bf16 group-128 scales of any sign);
+// "vLLM Quantization", section "Key points" (decode waits on memory); W4A8
+// per "int8 activations (W4A8) ...", section "Under the hood".
+//
+// Design (GB300):
+//  * Clusters of two CTAs, one CTA per SM. The output rows are cut into
+//    equal contiguous ranges, one per cluster; CTA q of the pair takes K half
+//    q of every row in the range, so each CTA stages only half of the
+//    activations (as MMA fragments) and the two halves meet once per chunk
+//    through distributed shared memory. Nothing goes through global memory
+//    but the weights, the scales, x and y.
+//  * A range is streamed in chunks of H <= 256 rows (one TMA box high). A
+//    producer warp keeps a deep ring of [H rows x one 128-code group] stages
+//    in flight (about 100-150 KB per SM) plus the chunk's scale box.
+//  * 16 consumer warps: a warp owns a 32-row tile of the chunk (two m16 MMA
+//    tiles sharing the activation fragments) and every ksplit-th group of the
+//    CTA's half; unpack by code pairing (wq_unpack.cuh), swap-AB m16n8k16,
+//    fp32 accumulators with the group scale applied per group.
+//  * Per chunk: the warps of a tile reduce in shared memory in a fixed order;
+//    each CTA pushes its sums of the rows its peer finalises into the peer's
+//    inbox (remote 16-byte stores) and arrives on the peer's "ready" barrier;
+//    each CTA then writes half the rows. A "consumed" arrival frees the inbox.
+//  * Programmatic dependent launch: the kernel lets the next one in the
+//    stream launch at once; the producer streams weights and scales (never
+//    written by these kernels) right away, the consumers wait for the
+//    previous kernel before reading activations or writing outputs.
+// All waits are bounded (WQ_ETIMEOUT on expiry).
+#include "wq_device.cuh"
+#include "wq_internal.h"
+#include "wq_unpack.cuh"
+
+namespace wq {
+namespace {
+
+using namespace unpack;
+
+constexpr int kCWarps = 16;                      // consumer warps
+constexpr int kThreads2 = (kCWarps + 1) * 32;    // + one producer warp
+constexpr int kTileRows = 32;                    // rows per warp tile
+constexpr int kMaxH = 256;                       // rows per chunk (TMA box limit)
+constexpr int kMaxStages = 16;
+constexpr int kXBatch = 3;                       // activation jobs a warp loads at once
+constexpr size_t kSmemCap = 227 * 1024 - 1024;   // dynamic smem budget (alignment slack)
+
+struct D2Params {
+  const uint16_t* x;   // bf16 [M, K] (WNA16)
+  const int8_t* xq;    // int8 [M, K] (W4A8)
+  const float* sx;     // [M] (W4A8)
+  int64_t M, N, K;
+  int G, Gh;           // groups, groups per K half
+  int C;               // clusters
+  int H, nchunk, T;    // chunk rows, chunks per range, 32-row tiles per chunk
+  int ksplit;          // consumer warps per tile (each takes every ksplit-th group)
+  int NS;              // ring stages
+  int sbox, sx0;       // scale box width, and the box start of each half (x0 of half q = q * sx0)
+  uint16_t* y;
+  unsigned* status;
+};
+
+// ---- cluster helpers (inline PTX) -------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a barrier that the peer CTA arrives on (cluster scope).
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+__device__ __forceinline__ void st_peer_v4(uint32_t cluster_addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+// Programmatic dependent launch: let the next kernel of the stream start
+// launching, and wait for the previous one (both no-ops without such a
+// neighbour).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// The 32 activations of a staged job, from their raw bf16 or int8 words.
+template <bool kInt8>
+__device__ __forceinline__ void raw_to_float(const uint4 (&r)[4], float (&v)[32]) {
+  if constexpr (!kInt8) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint32_t wv[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[8 * c + 2 * e] = __uint_as_float(wv[e] << 16);
+        v[8 * c + 2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint32_t wv[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        v[16 * c + e] = static_cast<float>(static_cast<int8_t>((wv[e >> 2] >> (8 * (e & 3))) & 0xFFu));
+    }
+  }
+}
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory");
+}
+
+template <int B>
+__device__ __forceinline__ void unpack_quad2(const uint32_t (&w)[B], int i2, uint32_t (&r)[4]) {
+  constexpr uint32_t kMagic = uses_fp16<B>() ? 0x64006400u : 0x43004300u;
+  constexpr uint32_t kM = (1u << B) - 1u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const PairSpec sp = pair_spec<B>(4 * i2 + q);
+    const uint32_t mask = (kM << sp.olo) | (kM << (16 + sp.ohi));
+    r[q] = lop3_and_or(slice_window<B>(w, sp.s), mask, kMagic);
+  }
+}
+
+// Shared-memory carve-up, identical on host (planning) and device.
+struct D2Smem {
+  size_t ring, slot, sbuf, xs, corr, scl, part, inbox, bars, total;
+};
+__host__ __device__ inline D2Smem d2_smem(int B, int NT, int T, int Gh, int sbox, int NS) {
+  D2Smem s{};
+  auto al = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
+  s.slot = al(static_cast<size_t>(T) * kTileRows * 16 * B, 1024);
+  s.ring = 0;
+  s.sbuf = s.ring + NS * s.slot;
+  s.xs = al(s.sbuf + 2 * static_cast<size_t>(T) * kTileRows * sbox * 2, 128);
+  s.corr = s.xs + static_cast<size_t>(NT) * Gh * 4 * 32 * 16;
+  s.scl = s.corr + static_cast<size_t>(NT) * 8 * Gh * 4;
+  s.part = al(s.scl + static_cast<size_t>(NT) * 8 * Gh * 4, 16);
+  s.inbox = s.part + static_cast<size_t>(T) * kTileRows * NT * 8 * 4;
+  s.bars = al(s.inbox + static_cast<size_t>(T) * (kTileRows / 2) * NT * 8 * 4, 8);
+  s.total = s.bars + (2 * kMaxStages + 4) * 8;
+  return s;
+}
+
+template <int B, int NT, bool kInt8>
+__global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                              const __grid_constant__ CUtensorMap smap,
+                                                              const D2Params p) {
+  constexpr bool kF16 = uses_fp16<B>();
+  constexpr int kTok = NT * 8;  // token columns of the partial-sum buffer
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ volatile int s_abort;
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const int Gh = p.Gh, T = p.T, NS = p.NS, ksplit = p.ksplit, H = p.H;
+  const D2Smem L = d2_smem(B, NT, T, Gh, p.sbox, NS);
+  uint8_t* ring = base + L.ring;
+  uint16_t* sbuf = reinterpret_cast<uint16_t*>(base + L.sbuf);
+  uint4* xs4 = reinterpret_cast<uint4*>(base + L.xs);
+  float* corr = reinterpret_cast<float*>(base + L.corr);
+  float* scl = reinterpret_cast<float*>(base + L.scl);
+  float* part = reinterpret_cast<float*>(base + L.part);    // this CTA's sums, [T*32 rows][kTok]
+  float* inbox = reinterpret_cast<float*>(base + L.inbox);  // the peer's sums of our half, [T*16][kTok]
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + L.bars);  // [kMaxStages]
+  uint64_t* empty = full + kMaxStages;                           // [kMaxStages]
+  uint64_t* cdone = empty + kMaxStages;  // [2]: consumers done with scale buffer k % 2
+  uint64_t* rbar = cdone + 2;            // the peer's sums of the chunk are ready
+  uint64_t* dbar = rbar + 1;             // the peer has read our sums of the chunk
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t q = cluster_rank();  // K half of this CTA
+  const uint32_t peer = q ^ 1u;
+  const int64_t cid = cluster_id_x();
+  const int64_t r0 = cid * p.N / p.C, r1 = (cid + 1) * p.N / p.C;  // the pair's rows
+  const int nck = static_cast<int>((r1 - r0 + H - 1) / H);      // chunks (the same in both CTAs)
+  const int gbase = static_cast<int>(q) * Gh;                    // first group of this half
+  const int scol0 = static_cast<int>(q) * p.sx0;                 // scale box start column
+  const int sbox_elems = T * kTileRows * p.sbox;
+  const uint32_t stage_bytes = static_cast<uint32_t>(H) * 16u * B;
+  const uint32_t scale_bytes = static_cast<uint32_t>(H) * p.sbox * 2u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], T);  // the T warps (one per tile) that read a stage
+    }
+    mbar_init(&cdone[0], kCWarps);
+    mbar_init(&cdone[1], kCWarps);
+    mbar_init(rbar, 1);
+    mbar_init(dbar, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  cluster_sync_all();  // the peer's barriers exist before anything arrives on them
+  if (threadIdx.x == 0) griddep_launch_dependents();
+
+  if (warp == kCWarps) {
+    // ---- producer: chunk k = rows r0 + k H .. + H - 1; stage = one group of
+    // this CTA's K half; the chunk's first stage also brings its scale box
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool stop = false;
+      for (int k = 0; k < nck && !stop; ++k) {
+        const int rc = static_cast<int>(r0 + static_cast<int64_t>(k) * H);
+        if (k >= 2 && !mbar_wait_bounded(&cdone[k & 1], ((k >> 1) - 1) & 1)) {
+          record_status(p.status, kStatusTimeout);
+          s_abort = 1;
+          break;
+        }
+        for (int gl = 0; gl < Gh; ++gl, ++it) {
+          const uint32_t s = it % NS;
+          if (s_abort || (it >= static_cast<uint32_t>(NS) && !mbar_wait_bounded(&empty[s], ((it / NS) - 1) & 1))) {
+            record_status(p.status, kStatusTimeout);
+            s_abort = 1;
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], stage_bytes + (gl == 0 ? scale_bytes : 0u));
+          tma_load_2d(ring + s * L.slot, &wmap, (gbase + gl) * 4 * B, rc, &full[s]);
+          if (gl == 0) tma_load_2d(sbuf + (k & 1) * sbox_elems, &smap, scol0, rc, &full[s]);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- consumers
+    const bool active = warp < T * ksplit;
+    const int tile = warp % T, kr = warp / T;
+    const int g = lane >> 2, t = lane & 3;
+
+    // activation fragments of this K half, built once while the producer
+    // streams weights. The activations are the previous kernel's output:
+    // wait for it first (no-op without a programmatic predecessor). Each warp
+    // issues the loads of up to kXBatch jobs before building any fragments.
+    griddep_wait();
+    for (int j0 = warp; j0 < NT * Gh; j0 += kXBatch * kCWarps) {
+      uint4 rawv[kXBatch][4];
+#pragma unroll
+      for (int b = 0; b < kXBatch; ++b) {
+        const int job = j0 + b * kCWarps;
+        const int gl = job % Gh, j = job / Gh;
+        const int64_t tok = j * 8 + g;
+        const bool valid = job < NT * Gh && tok < p.M;
+        const int64_t k0 = static_cast<int64_t>(gbase + gl) * 128 + 32 * t;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) rawv[b][c] = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+          if constexpr (kInt8) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.xq + tok * p.K + k0);
+            rawv[b][0] = src[0];
+            rawv[b][1] = src[1];
+          } else {
+            const uint4* src = reinterpret_cast<const uint4*>(p.x + tok * p.K + k0);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) rawv[b][c] = src[c];
+          }
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kXBatch; ++b) {
+        const int job = j0 + b * kCWarps;
+        if (job >= NT * Gh) break;  // warp-uniform
+        const int gl = job % Gh, j = job / Gh;
+        float xv[32];
+        raw_to_float<kInt8>(rawv[b], xv);
+        uint32_t frag[16];
+        float cr, sb;
+        make_fragments<B>(xv, frag, cr, sb);
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2)
+          xs4[((j * Gh + gl) * 4 + i2) * 32 + lane] =
+              make_uint4(frag[4 * i2], frag[4 * i2 + 1], frag[4 * i2 + 2], frag[4 * i2 + 3]);
+        if (t == 0) {
+          corr[(j * 8 + g) * Gh + gl] = cr;
+          scl[(j * 8 + g) * Gh + gl] = sb;
+        }
+      }
+    }
+    consumer_sync();
+
+    bool stop = false;  // warp-uniform
+    for (int k = 0; k < nck; ++k) {
+      const int64_t rc = r0 + static_cast<int64_t>(k) * H;
+      const uint16_t* sbk = sbuf + (k & 1) * sbox_elems;
+      float acc[NT][2][4];
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[j][h][e] = 0.0f;
+
+      if (active && !stop) {
+        const int rowt = tile * kTileRows + g;  // rows rowt + {0, 8, 16, 24} of the chunk
+        for (int gl = kr; gl < Gh; gl += ksplit) {
+          const uint32_t it = static_cast<uint32_t>(k) * Gh + gl, s = it % NS;
+          if (!__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&full[s], (it / NS) & 1))) {
+            if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
+            s_abort = 1;
+            stop = true;
+            break;
+          }
+          const uint32_t* st = reinterpret_cast<const uint32_t*>(ring + s * L.slot);
+          uint32_t w0[B], w1[B], w2[B], w3[B];
+          load_slice<B>(st, rowt, t, w0);
+          load_slice<B>(st, rowt + 8, t, w1);
+          load_slice<B>(st, rowt + 16, t, w2);
+          load_slice<B>(st, rowt + 24, t, w3);
+          __syncwarp();  // every lane has its words: the slot may be refilled
+          if (lane == 0) mbar_arrive(&empty[s]);
+          const int scol = gbase + gl - scol0;
+          float sc[4];
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) sc[qq] = bf16_bits_to_float(sbk[(rowt + 8 * qq) * p.sbox + scol]);
+          float c[NT][2][4];
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) c[j][h][e] = 0.0f;
+#pragma unroll
+          for (int i2 = 0; i2 < 4; ++i2) {
+            uint32_t a0[4], a1[4], a2[4], a3[4];
+            unpack_quad2<B>(w0, i2, a0);
+            unpack_quad2<B>(w1, i2, a1);
+            unpack_quad2<B>(w2, i2, a2);
+            unpack_quad2<B>(w3, i2, a3);
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              const uint4 bv = xs4[((j * Gh + gl) * 4 + i2) * 32 + lane];
+              mma16<kF16>(c[j][0], a0[0], a1[0], a0[1], a1[1], bv.x, bv.y);
+              mma16<kF16>(c[j][1], a2[0], a3[0], a2[1], a3[1], bv.x, bv.y);
+              mma16<kF16>(c[j][0], a0[2], a1[2], a0[3], a1[3], bv.z, bv.w);
+              mma16<kF16>(c[j][1], a2[2], a3[2], a2[3], a3[3], bv.z, bv.w);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const int ti0 = (j * 8 + 2 * t) * Gh + gl, ti1 = ti0 + Gh;
+            const float cr0 = corr[ti0], cr1 = corr[ti1], sl0 = scl[ti0], sl1 = scl[ti1];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              acc[j][h][0] = fmaf(sc[2 * h], fmaf(sl0, c[j][h][0], -cr0), acc[j][h][0]);
+              acc[j][h][1] = fmaf(sc[2 * h], fmaf(sl1, c[j][h][1], -cr1), acc[j][h][1]);
+              acc[j][h][2] = fmaf(sc[2 * h + 1], fmaf(sl0, c[j][h][2], -cr0), acc[j][h][2]);
+              acc[j][h][3] = fmaf(sc[2 * h + 1], fmaf(sl1, c[j][h][3], -cr1), acc[j][h][3]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cdone[k & 1]);  // done with scale buffer k % 2
+
+      // the peer has consumed its inbox of the previous chunk: it may be
+      // written again
+      if (k >= 1 && !__all_sync(0xFFFFFFFFu, mbar_wait_cluster_bounded(dbar, (k - 1) & 1))) {
+        if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
+        s_abort = 1;
+        stop = true;
+      }
+      // reduce the ksplit warps of each tile, in a fixed order
+      for (int r = 0; r < ksplit; ++r) {
+        if (active && kr == r) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int rl = tile * kTileRows + g + 16 * h + 8 * (e >> 1);
+                float* d = part + rl * kTok + j * 8 + 2 * t + (e & 1);
+                *d = (r == 0) ? acc[j][h][e] : *d + acc[j][h][e];
+              }
+        }
+        consumer_sync();
+      }
+      // push our sums of the rows the peer finalises into its inbox (remote
+      // 16-byte stores, no waiting), then tell it they are there
+      const int half_rows = T * (kTileRows / 2);
+      {
+        const uint32_t pin = map_peer(smem_u32(inbox), peer);
+        const int nvec = half_rows * (kTok / 4);
+        for (int e = threadIdx.x; e < nvec; e += kCWarps * 32) {
+          const int rr = e / (kTok / 4), c4 = e % (kTok / 4);
+          const float4 v = *reinterpret_cast<const float4*>(part + (static_cast<int>(peer) * half_rows + rr) * kTok + 4 * c4);
+          st_peer_v4(pin + 16u * static_cast<uint32_t>(rr * (kTok / 4) + c4), v);
+        }
+      }
+      consumer_sync();
+      if (threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(rbar), peer));
+      // the peer's sums of our rows are in our inbox: combine, write y
+      const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait_cluster_bounded(rbar, k & 1));
+      if (!ready && threadIdx.x == 0) {
+        record_status(p.status, kStatusTimeout);
+        s_abort = 1;
+      }
+      if (ready) {
+        for (int e = threadIdx.x; e < half_rows * kTok; e += kCWarps * 32) {
+          const int rr = e % half_rows, tok = e / half_rows;
+          const int rl = static_cast<int>(q) * half_rows + rr;
+          const int64_t row = rc + rl;
+          if (tok < p.M && row < r1) {
+            float v = part[rl * kTok + tok] + inbox[rr * kTok + tok];
+            if constexpr (kInt8) v *= p.sx[tok];
+            p.y[tok * p.N + row] = float_to_bf16_bits_rn(v);
+          }
+        }
+      }
+      // our inbox has been read: the peer may fill it for the next chunk.
+      // After the last chunk nothing is sent any more, so no arrival: every
+      // remote operation of the peer on this CTA (inbox stores, the "ready"
+      // arrival) precedes the "ready" wait above, and the CTA may exit.
+      if (k + 1 < nck) {
+        consumer_sync();
+        if (threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(dbar), peer));
+      }
+    }
+  }
+  __syncthreads();
+}
+
+struct D2Plan {
+  D2Params prm;
+  int NT;
+  size_t smem;
+  bool ok;
+};
+
+D2Plan make_d2plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
+  D2Plan pl{};
+  pl.ok = false;
+  // K % 1024 == 0: the scale rows are 16-byte multiples (TMA) and each K half
+  // is a whole number of groups
+  if (M < 1 || M > 16 || N < 1 || K < 1024 || K % 1024 != 0 || sm_count < 2) return pl;
+  if (N >= (int64_t(1) << 31)) return pl;
+  D2Params& p = pl.prm;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.G = static_cast<int>(K / 128);
+  p.Gh = p.G / 2;
+  const int64_t max_c = sm_count / 2;
+  const int64_t by_rows = (N + kTileRows - 1) / kTileRows;  // at least a 32-row tile per pair
+  p.C = static_cast<int>(by_rows < max_c ? by_rows : max_c);
+  const int64_t rows_max = (N + p.C - 1) / p.C;
+  p.nchunk = static_cast<int>((rows_max + kMaxH - 1) / kMaxH);
+  p.H = static_cast<int>((rows_max + p.nchunk - 1) / p.nchunk);
+  p.T = (p.H + kTileRows - 1) / kTileRows;
+  p.sx0 = (p.Gh / 8) * 8;
+  p.sbox = ((p.G - p.sx0 + 7) / 8) * 8;  // covers [0, Gh) and [Gh, G) from their box starts
+  if (p.sbox < p.Gh || p.sbox > 256) return pl;
+  pl.NT = M <= 8 ? 1 : 2;
+  // Stage gl of a chunk belongs to the warps with kr = gl % ksplit. With
+  // ksplit dividing both Gh and the ring depth NS, slot s always belongs to
+  // the warps kr = s % ksplit, so whoever waits on a slot's "full" barrier
+  // has consumed that slot's previous phase (a parity wait is only sound then).
+  p.ksplit = 0;
+  p.NS = 0;
+  for (int ks = kCWarps / p.T; ks >= 1 && p.NS == 0; --ks) {
+    if (ks > p.Gh || p.Gh % ks != 0) continue;
+    for (int ns = (kMaxStages / ks) * ks; ns >= ks && ns >= 2; ns -= ks) {
+      if (d2_smem(bits, pl.NT, p.T, p.Gh, p.sbox, ns).total <= kSmemCap) {
+        p.ksplit = ks;
+        p.NS = ns;
+        break;
+      }
+    }
+  }
+  if (p.NS < 2 || p.ksplit < 1) return pl;
+  pl.smem = d2_smem(bits, pl.NT, p.T, p.Gh, p.sbox, p.NS).total + 1024;  // + base alignment
+  pl.ok = true;
+  return pl;
+}
+
+template <int B, int NT, bool kInt8>
+cudaError_t d2launch(const Ctx& c, const CUtensorMap& wmap, const CUtensorMap& smap, const D2Plan& pl) {
+  static int configured[64] = {};  // dynamic smem opted in so far, per device
+  if (c.device < 0 || c.device >= 64) return cudaErrorInvalidDevice;
+  auto kern = decode2_kernel<B, NT, kInt8>;
+  if (configured[c.device] < static_cast<int>(pl.smem)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
+    if (e != cudaSuccess) return e;
+    configured[c.device] = static_cast<int>(pl.smem);
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pl.prm.C), 1, 1);
+  cfg.blockDim = dim3(kThreads2, 1, 1);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel of the stream finishes: the kernel
+  // reads only weights and scales before griddepcontrol.wait
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, wmap, smap, pl.prm);
+}
+
+template <bool kInt8>
+cudaError_t d2launch_b(const Ctx& c, int bits, const CUtensorMap& wmap, const CUtensorMap& smap, const D2Plan& pl) {
+  if constexpr (kInt8) {
+    if (bits != 4) return cudaErrorInvalidValue;
+    return pl.NT == 1 ? d2launch<4, 1, true>(c, wmap, smap, pl) : d2launch<4, 2, true>(c, wmap, smap, pl);
+  } else {
+#define WQ_D2(BB) \
+  case BB: return pl.NT == 1 ? d2launch<BB, 1, false>(c, wmap, smap, pl) : d2launch<BB, 2, false>(c, wmap, smap, pl);
+    switch (bits) {
+      WQ_D2(2)
+      WQ_D2(3)
+      WQ_D2(4)
+      WQ_D2(5)
+      WQ_D2(6)
+      WQ_D2(7)
+      WQ_D2(8)
+      default: return cudaErrorInvalidValue;
+    }
+#undef WQ_D2
+  }
+}
+
+}  // namespace
+
+bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
+  return bits >= 2 && bits <= 8 && make_d2plan(M, N, K, bits, sm_count).ok;
+}
+
+bool decode2_shape(int64_t M, int64_t K) { return M >= 1 && M <= 16 && K >= 1024 && K % 1024 == 0; }
+
+cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a) {
+  const bool int8 = a.mode == GemvMode::kW4a8;
+  if (a.mode != GemvMode::kWna16 && !int8) return cudaErrorInvalidValue;
+  const D2Plan pl = make_d2plan(a.M, a.N, a.K, a.bits, c.sm_count);
+  if (!pl.ok) return cudaErrorInvalidValue;
+  D2Plan q = pl;
+  q.prm.x = a.x;
+  q.prm.xq = a.xq;
+  q.prm.sx = a.sx;
+  q.prm.y = a.y;
+  q.prm.status = c.status;
+  CUtensorMap wmap, smap;
+  const uint64_t words = static_cast<uint64_t>(a.K) * a.bits / 32;
+  if (!make_tmap_u32_2d(&wmap, a.packed, words, static_cast<uint64_t>(a.N), 4u * a.bits,
+                        static_cast<uint32_t>(pl.prm.H)))
+    return cudaErrorInvalidValue;
+  if (!make_tmap_bf16_2d(&smap, a.scales, static_cast<uint64_t>(pl.prm.G), static_cast<uint64_t>(a.N),
+                         static_cast<uint32_t>(pl.prm.sbox), static_cast<uint32_t>(pl.prm.H)))
+    return cudaErrorInvalidValue;
+  return int8 ? d2launch_b<true>(c, a.bits, wmap, smap, q) : d2launch_b<false>(c, a.bits, wmap, smap, q);
+}
+
+}  // namespace wq

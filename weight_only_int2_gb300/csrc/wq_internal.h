@@ -95,15 +95,25 @@ inline bool use_prefill(int64_t M, int64_t N, int64_t K, int bits) {
   return M >= kPrefillMinTokens && prefill_supported(M, N, K, bits);
 }
 
-// Routes a weight-streaming GEMM (few tokens) to the persistent decode kernel
-// when it applies, else to the chunked kernel.
+// Decode by CTA pairs (M <= 16, K % 1024 == 0): no workspace, no grid-wide
+// synchronisation. Modes kWna16 and kW4a8.
+bool decode2_shape(int64_t M, int64_t K);
+bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count);
+cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a);
+
+// Routes a weight-streaming GEMM (few tokens): the CTA-pair decode kernel
+// when it applies, else the persistent split-K decode kernel, else the
+// chunked kernel.
 inline cudaError_t launch_stream_gemm(const Ctx& c, const GemvArgs& a) {
+  if (a.mode != GemvMode::kW4a8GroupAcc && decode2_supported(a.M, a.N, a.K, a.bits, c.sm_count))
+    return launch_decode2(c, a);
   return decode_supported(a.M, a.N, a.K, a.bits, c.sm_count) ? launch_decode(c, a) : launch_gemv(c, a);
 }
 
-// Workspace of the path a shape takes: none for the tensor-core GEMM.
+// Workspace of the path a shape takes: none for the tensor-core GEMM and the
+// CTA-pair decode kernel.
 inline size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  if (M >= kPrefillMinTokens) return 0;
+  if (M >= kPrefillMinTokens || decode2_shape(M, K)) return 0;
   const size_t a = gemv_workspace_bytes(M, N, K), b = decode_workspace_bytes(M, N);
   return a > b ? a : b;
 }
