@@ -445,15 +445,14 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           }
         }
       }
-      // our inbox has been read: the peer may fill it for the next chunk.
-      // After the last chunk nothing is sent any more, so no arrival: every
-      // remote operation of the peer on this CTA (inbox stores, the "ready"
-      // arrival) precedes the "ready" wait above, and the CTA may exit.
-      if (k + 1 < nck) {
-        consumer_sync();
-        if (threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(dbar), peer));
-      }
+      consumer_sync();  // our inbox has been read: the peer may fill it again
+      if (threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(dbar), peer));
     }
+    // The pair leaves together: waiting for the peer's last arrival (measured:
+    // letting each CTA leave as soon as its rows are written is slower when
+    // the next kernel launches programmatically).
+    if (nck >= 1 && !mbar_wait_cluster_bounded(dbar, (nck - 1) & 1) && threadIdx.x == 0)
+      record_status(p.status, kStatusTimeout);
   }
   __syncthreads();
 }
