@@ -50,7 +50,7 @@ def _peaks():
 
 def _kernel_hash():
     h = hashlib.sha256()
-    for f in ("decode.cu", "wq_unpack.cuh", "wq_device.cuh"):
+    for f in ("decode2.cu", "wq_unpack.cuh", "wq_device.cuh"):
         h.update(open(os.path.join(ROOT, "weight_only_int2_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -268,7 +268,7 @@ def run_ours(args, rank, world, dist):
         traffic = round(tr["dram_bytes_per_launch"] * (step_bytes / len(cases)) / ref_bytes)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": traffic,
-                "kernel": "decode_kernel (persistent, warp MMA + TMA weight stream)",
+                "kernel": "decode2_kernel (CTA pairs over K halves, TMA weight ring, warp MMA)",
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": "N*K*bits/8 packed weight bytes",
                 "duration": "CUDA events around back-to-back graph replays of the step, divided by launches"}
