@@ -4,7 +4,9 @@ One step = one pass of the decode sweep: bits {5,6,7} x N {5120,17408} x
 M {1,4,16}, K = 5120, group 128 (18 GEMMs, each on its own copy of the packed
 weights, so a step streams ~0.78 GB of distinct weights: inputs larger than
 L2). The value is whole-job decode throughput in GB/s of packed weight bytes.
-A prefill GEMM (M = 8192) is timed separately and reported under "prefill".
+The other rows (prefill sweep, W4A8, 8-bit lm_head, embedding gather, the
+64-layer mixed-bit stack) are timed separately and reported under "extras",
+each against its roofline.
 
     python bench.py [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -35,7 +37,6 @@ K_DIM = 5120
 DECODE_BITS = (5, 6, 7)
 DECODE_N = (5120, 17408)
 DECODE_M = (1, 4, 16)
-PREFILL = dict(M=8192, N=17408, K=5120, bits=6)
 WORKLOAD = ("decode sweep: bits {5,6,7} x N {5120,17408} x M {1,4,16}, K=5120, group=128, "
             "x bf16 N(0,1), codes uniform, scales 0.01|N(0,1)| with random sign")
 
@@ -250,10 +251,10 @@ def run_ours(args, rank, world, dist):
                 e2e_ms.append(a.elapsed_time(b))
     e2e_value = world * step_bytes / (float(np.mean(e2e_ms)) * 1e-3) / 1e9
 
-    # ---- prefill (separate timed region; reported, not the headline)
-    prefill = None
+    # ---- the other rows (separate timed regions; reported, not the headline)
+    extras = None
     if not args.no_prefill:
-        prefill = _time_prefill(wq, torch, stream)
+        extras = _time_extras(wq, torch, stream)
 
     hbm, bf16, bf16_sus, src = _peaks()
     # average launch duration = step time / launches (back-to-back graph
@@ -274,37 +275,148 @@ def run_ours(args, rank, world, dist):
                 "duration": "CUDA events around back-to-back graph replays of the step, divided by launches"}
     return dict(value=value, ms_per_step=ms_per_step, cases=case_rows, e2e=dict(
         value=round(e2e_value, 1), unit="GB/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
-        prefill=prefill, roofline=roofline, clocks=clk.summary(), launches=len(cases) * args.steps,
+        extras=extras, roofline=roofline, clocks=clk.summary(), launches=len(cases) * args.steps,
         bf16_peak=(bf16, bf16_sus, src))
 
 
-def _time_prefill(wq, torch, stream):
-    import wq_inputs as I
-
-    M, N, K, bits = PREFILL["M"], PREFILL["N"], PREFILL["K"], PREFILL["bits"]
-    codes = torch.from_numpy(I.make_codes(N, K, bits, 77)).cuda()
-    s = torch.from_numpy(I.make_scales(N, K // 128, 78).view(np.int16)).view(torch.bfloat16).cuda()
-    packed, s = wq.wna16_repack(codes, s, bits)
-    del codes
-    x = torch.from_numpy(I.make_x(M, K, 79).view(np.int16)).view(torch.bfloat16).cuda()
-    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+def _event_ms(torch, stream, fn, reps):
+    """Average device time of fn() over reps calls on stream (CUDA events)."""
     with torch.cuda.stream(stream):
-        for _ in range(2):
-            wq.wna16_gemm(x, packed, s, N, K, bits, y=y)
+        fn()
         stream.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        reps = 3
         a.record(stream)
         for _ in range(reps):
-            wq.wna16_gemm(x, packed, s, N, K, bits, y=y)
+            fn()
         b.record(stream)
         stream.synchronize()
-    ms = a.elapsed_time(b) / reps
-    tflops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
-    _, bf16, bf16_sus, src = _peaks()
-    return {"config": f"M={M} N={N} K={K} bits={bits}", "ms": round(ms, 3), "TFLOPS": round(tflops, 1),
-            "peak_TFLOPS": bf16, "frac": round(tflops / bf16, 4), "peak_source": src}
+    return a.elapsed_time(b) / reps
+
+
+def _graph_ms(torch, stream, fn, reps):
+    """Average device time of one replay of a CUDA graph that captured fn()."""
+    with torch.cuda.stream(stream):
+        fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        for _ in range(2):
+            g.replay()
+        stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        stream.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def _rand_layer(wq, torch, N, K, bits, gen):
+    """Random codes (uniform) and scales (0.01 |N(0,1)|, random sign) on the
+    device, repacked; for timing only (parity runs on the seeded host inputs)."""
+    codes = torch.randint(0, 1 << bits, (N, K), dtype=torch.uint8, device="cuda", generator=gen)
+    sc = torch.randn(N, K // 128, device="cuda", generator=gen) * 0.01
+    packed, s = wq.wna16_repack(codes, sc.to(torch.bfloat16), bits)
+    del codes
+    return packed, s
+
+
+def _time_extras(wq, torch, stream):
+    """The other rows of the scope table, each against its roofline: prefill
+    sweep, W4A8, the 8-bit lm_head, the embedding gather and the 64-layer
+    mixed-bit stack (timed as one CUDA graph)."""
+    hbm, bf16, _, src = _peaks()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1234)
+    K = 5120
+    out = {"peak_source": src}
+
+    def gbs(nbytes, ms):
+        v = nbytes / (ms * 1e-3) / 1e9
+        return {"ms": round(ms, 4), "GBps": round(v, 1), "frac": round(v / hbm, 4)}
+
+    def tfl(flops, ms):
+        v = flops / (ms * 1e-3) / 1e12
+        return {"ms": round(ms, 4), "TFLOPS": round(v, 1), "frac": round(v / bf16, 4)}
+
+    # prefill sweep: M in {2048, 8192} x bits in {5,6,7,8}, N = 17408
+    N = 17408
+    rows = []
+    for bits in (5, 6, 7, 8):
+        packed, s = _rand_layer(wq, torch, N, K, bits, gen)
+        for M in (2048, 8192):
+            x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
+            y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+            ms = _event_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, N, K, bits, y=y), 3)
+            rows.append(dict(bits=bits, M=M, **tfl(2.0 * M * N * K, ms)))
+        del packed, s
+    out["prefill"] = rows
+
+    # W4A8 (int8 activations quantized per token inside the call)
+    packed, s = _rand_layer(wq, torch, N, K, 4, gen)
+    rows = []
+    for M in (1, 512, 8192):
+        x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        if M == 1:
+            ms = _graph_ms(torch, stream, lambda: wq.w4a8_gemm(x, packed, s, N, K, y=y), 200)
+            rows.append(dict(M=M, **gbs(N * K * 4 / 8, ms)))
+        else:
+            ms = _event_ms(torch, stream, lambda: wq.w4a8_gemm(x, packed, s, N, K, y=y), 3)
+            rows.append(dict(M=M, **tfl(2.0 * M * N * K, ms)))
+    out["w4a8"] = rows
+    del packed, s
+
+    # lm_head: 8-bit, N = 248320 (1.27 GB packed), and the gather from the same table
+    V = 248320
+    packed, s = _rand_layer(wq, torch, V, K, 8, gen)
+    rows = []
+    for M in (1, 4096):
+        x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
+        y = torch.empty(M, V, dtype=torch.bfloat16, device="cuda")
+        if M == 1:
+            ms = _graph_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, V, K, 8, y=y), 20)
+            rows.append(dict(M=M, **gbs(V * K, ms)))
+        else:
+            ms = _event_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, V, K, 8, y=y), 3)
+            rows.append(dict(M=M, **tfl(2.0 * M * V * K, ms)))
+    out["lm_head"] = rows
+    T = 4096
+    ids = torch.randint(0, V, (T,), dtype=torch.int32, device="cuda", generator=gen)
+    ms = _graph_ms(torch, stream, lambda: wq.qembed_gather(ids, packed, s, V, K, 8), 100)
+    moved = T * (K + 2 * K // 128 + 2 * K + 4)  # packed row + scales in, bf16 row out, id
+    out["gather"] = dict(T=T, bytes_moved=moved, **gbs(moved, ms))
+    del packed, s
+
+    # 64-layer stack: layers 0-9 and 54-63 at 7 bits, 10-53 alternating 5 / 6
+    layers = []
+    for li in range(64):
+        bits = 7 if (li < 10 or li >= 54) else (5 if (li - 10) % 2 == 0 else 6)
+        packed, s = _rand_layer(wq, torch, N, K, bits, gen)
+        layers.append((bits, packed, s))
+    stack_bytes = sum(N * K * b / 8 for b, _, _ in layers)
+    rows = []
+    for M in (1, 4096):
+        x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
+        ys = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+
+        def stack():
+            for li, (b, pk, sc) in enumerate(layers):
+                wq.wna16_gemm(x, pk, sc, N, K, b, y=ys[li & 1])
+
+        ms = _graph_ms(torch, stream, stack, 3 if M > 1 else 10)
+        if M == 1:
+            rows.append(dict(M=M, layers=64, packed_bytes=int(stack_bytes), **gbs(stack_bytes, ms)))
+        else:
+            rows.append(dict(M=M, layers=64, **tfl(2.0 * M * N * K * 64, ms)))
+    out["stack"] = rows
+    del layers
+    torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------------------------- oracle arms
@@ -372,7 +484,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-prefill", "--no-extras", dest="no_prefill", action="store_true",
+                    help="skip the other rows (prefill, W4A8, lm_head, gather, stack)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--case", type=str, default=None,
@@ -413,7 +526,7 @@ def main():
                            "l2": "inputs larger than L2: each step reads 0.78 GB of distinct packed weights",
                            "timing": "CUDA graph of one step, CUDA events between launches"},
                 "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
-                "gpu_launches": r["launches"], "clocks": r["clocks"], "prefill": r["prefill"],
+                "gpu_launches": r["launches"], "clocks": r["clocks"], "extras": r["extras"],
                 "cases": r["cases"]}
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -16,7 +16,8 @@
 //    but the weights, the scales, x and y.
 //  * A range is streamed in chunks of H <= 256 rows (one TMA box high). A
 //    producer warp keeps a deep ring of [H rows x one 128-code group] stages
-//    in flight (about 100-150 KB per SM) plus the chunk's scale box.
+//    in flight (about 100-150 KB per SM) plus the chunk's scale box (its own
+//    barrier: all consumer warps read it, whatever stages they own).
 //  * 16 consumer warps: a warp owns a 32-row tile of the chunk (two m16 MMA
 //    tiles sharing the activation fragments) and every ksplit-th group of the
 //    CTA's half; unpack by code pairing (wq_unpack.cuh), swap-AB m16n8k16,
@@ -175,7 +176,7 @@ __host__ __device__ inline D2Smem d2_smem(int B, int NT, int T, int Gh, int sbox
   s.part = al(s.scl + static_cast<size_t>(NT) * 8 * Gh * 4, 16);
   s.inbox = s.part + static_cast<size_t>(T) * kTileRows * NT * 8 * 4;
   s.bars = al(s.inbox + static_cast<size_t>(T) * (kTileRows / 2) * NT * 8 * 4, 8);
-  s.total = s.bars + (2 * kMaxStages + 4) * 8;
+  s.total = s.bars + (2 * kMaxStages + 6) * 8;
   return s;
 }
 
@@ -203,6 +204,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
   uint64_t* cdone = empty + kMaxStages;  // [2]: consumers done with scale buffer k % 2
   uint64_t* rbar = cdone + 2;            // the peer's sums of the chunk are ready
   uint64_t* dbar = rbar + 1;             // the peer has read our sums of the chunk
+  uint64_t* sfull = dbar + 1;            // [2]: scale box of chunk k landed in buffer k % 2
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t q = cluster_rank();  // K half of this CTA
@@ -225,6 +227,8 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
     mbar_init(&cdone[1], kCWarps);
     mbar_init(rbar, 1);
     mbar_init(dbar, 1);
+    mbar_init(&sfull[0], 1);
+    mbar_init(&sfull[1], 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -245,6 +249,10 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           s_abort = 1;
           break;
         }
+        // the chunk's scale box, on its own barrier: every consumer warp of
+        // the chunk reads it, whichever stages it owns
+        mbar_arrive_expect_tx(&sfull[k & 1], scale_bytes);
+        tma_load_2d(sbuf + (k & 1) * sbox_elems, &smap, scol0, rc, &sfull[k & 1]);
         for (int gl = 0; gl < Gh; ++gl, ++it) {
           const uint32_t s = it % NS;
           if (s_abort || (it >= static_cast<uint32_t>(NS) && !mbar_wait_bounded(&empty[s], ((it / NS) - 1) & 1))) {
@@ -253,9 +261,8 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
             stop = true;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], stage_bytes + (gl == 0 ? scale_bytes : 0u));
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
           tma_load_2d(ring + s * L.slot, &wmap, (gbase + gl) * 4 * B, rc, &full[s]);
-          if (gl == 0) tma_load_2d(sbuf + (k & 1) * sbox_elems, &smap, scol0, rc, &full[s]);
         }
       }
     }
@@ -328,6 +335,12 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[j][h][e] = 0.0f;
 
+      // the chunk's scales (every active warp waits on every chunk's phase)
+      if (active && !stop && !__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&sfull[k & 1], (k >> 1) & 1))) {
+        if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
+        s_abort = 1;
+        stop = true;
+      }
       if (active && !stop) {
         const int rowt = tile * kTileRows + g;  // rows rowt + {0, 8, 16, 24} of the chunk
         for (int gl = kr; gl < Gh; gl += ksplit) {
