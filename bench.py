@@ -142,6 +142,24 @@ def _make_case_inputs(wq, torch, bits, N, M, seed):
                 bytes=N * wq.packed_words_per_row(K_DIM, bits) * 4)
 
 
+def _max_over_ranks(v: float, dist, device) -> float:
+    """The maximum of v over all ranks (v itself without a process group)."""
+    if dist is None:
+        return float(v)
+    import torch
+
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _aggregate(step_bytes: float, ms_local: float, world: int, dist, device):
+    """Whole-job throughput of replicas: every rank moves step_bytes per step;
+    the job's step time is the slowest rank's. Returns (ms, GB/s)."""
+    ms = _max_over_ranks(ms_local, dist, device)
+    return ms, world * step_bytes / (ms * 1e-3) / 1e9
+
+
 def run_ours(args, rank, world, dist):
     import torch
 
@@ -219,12 +237,7 @@ def run_ours(args, rank, world, dist):
         graph_ev.replay()
     torch.cuda.synchronize()
     per_launch = [[evs[i].elapsed_time(evs[i + 1])] for i in range(len(cases))]
-    ms_per_step = t0.elapsed_time(t1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_per_step], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    ms_per_step, value = _aggregate(step_bytes, t0.elapsed_time(t1) / args.steps, world, dist, "cuda")
 
     case_rows = []
     for i, c in enumerate(cases):
@@ -249,7 +262,7 @@ def run_ours(args, rank, world, dist):
             stream.synchronize()
             if it >= args.warmup:
                 e2e_ms.append(a.elapsed_time(b))
-    e2e_value = world * step_bytes / (float(np.mean(e2e_ms)) * 1e-3) / 1e9
+    _, e2e_value = _aggregate(step_bytes, float(np.mean(e2e_ms)), world, dist, "cuda")
 
     # ---- the other rows (separate timed regions; reported, not the headline)
     extras = None
