@@ -222,3 +222,73 @@ def test_gather_empty():
 
 def test_status_word_clear_after_runs():
     wq.check_status()
+
+
+def test_w4a8_decode_quantizes_like_act_quant():
+    """Few tokens: the decode kernel quantizes the activations itself. With
+    half-way values (x / sx = k + 1/2), every code q - z = 1 and unit scales,
+    y is the exact integer sum of the int8 codes, so any difference in
+    rounding from the activation-quant definition shows up bit for bit."""
+    M, N, K = 3, 64, 1024
+    row = np.zeros((1, K), dtype=np.float32)
+    row[0, :8] = [127.0, 2.5, 3.5, -2.5, 0.5, 1.5, -0.5, 126.5]
+    row[0, 300:304] = [-4.5, 5.5, -6.5, 7.5]
+    x = np.zeros((M, K), dtype=np.uint16)
+    x[0] = I._to_bf16_bits(row)[0]
+    x[2] = I._to_bf16_bits(row * np.float32(2.0))[0]   # sx = 2: the same codes
+    q = np.full((N, K), 9, dtype=np.uint8)
+    s = np.full((N, K // 128), 0x3F80, dtype=np.uint16)  # bf16 1.0
+    packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(s), 4)
+    y = wq.w4a8_gemm(to_dev_bf16(x), packed, s_dev, N, K)
+    torch.cuda.synchronize()
+    y_ref, _, _ = O.w4a8_ref(x, q, s)
+    ref_bits = O.f32_to_bf16_bits_rne(y_ref.astype(np.float32))
+    assert np.array_equal(bf16_dev_to_bits(y), ref_bits)
+    assert np.all(bf16_dev_to_bits(y)[1] == 0)  # all-zero token
+
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_w4a8_decode_codes_bit_exact(M):
+    """Every int8 code of the in-kernel quantization, checked one by one:
+    row n of W is the zero point (8) except 9 at column n, unit scales, so
+    y[m, n] = RN32(sx[m] * xq[m, n]) rounded to bf16. Outlier activations
+    make the per-token scales differ widely."""
+    N = K = 1024
+    x = I.make_x_outliers(M, K, 500 + M)
+    q = np.full((N, K), 8, dtype=np.uint8)
+    q[np.arange(N), np.arange(N)] = 9
+    s = np.full((N, K // 128), 0x3F80, dtype=np.uint16)
+    packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(s), 4)
+    y = wq.w4a8_gemm(to_dev_bf16(x), packed, s_dev, N, K)
+    torch.cuda.synchronize()
+    xq, sx = O.act_quant_ref(x)
+    ref = O.f32_to_bf16_bits_rne((xq.astype(np.float32) * sx[:, None]).astype(np.float32))
+    assert np.array_equal(bf16_dev_to_bits(y), ref)
+
+
+@pytest.mark.parametrize("side", ["tiny", "huge"])
+def test_w4a8_decode_codes_extreme_scales(side):
+    """The in-kernel quantization at token scales far from 1: a subnormal sx
+    (activations near 2^-130), sx near 2^-101, 2^99 and 2^119. The diagonal
+    weight pattern with group scale 2^120 (tiny tokens) or 2^-120 (huge ones)
+    keeps y = RN32(xq * sx * s) a normal number, so every int8 code shows in
+    y bit for bit."""
+    N = K = 1024
+    exps = [-130, -124, -100] if side == "tiny" else [100, 120]
+    base = O.bf16_bits_to_f32(I.make_x_outliers(len(exps), K, 700))
+    rows = [base[i] * np.float32(2.0 ** e) for i, e in enumerate(exps)]
+    x = I._to_bf16_bits(np.stack(rows).astype(np.float32))
+    q = np.full((N, K), 8, dtype=np.uint8)
+    q[np.arange(N), np.arange(N)] = 9
+    s_val = 2.0 ** 120 if side == "tiny" else 2.0 ** -120
+    s = np.full((N, K // 128), O.f32_to_bf16_bits_rne(np.array([s_val], dtype=np.float32))[0], dtype=np.uint16)
+    packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(s), 4)
+    y = wq.w4a8_gemm(to_dev_bf16(x), packed, s_dev, N, K)
+    torch.cuda.synchronize()
+    xq, sx = O.act_quant_ref(x)
+    assert np.all(sx > 0)
+    if side == "tiny":
+        assert sx[0] < np.float32(2.0 ** -126)  # the subnormal case is exercised
+    sxs = (sx.astype(np.float64) * s_val).astype(np.float32)  # exact: a power-of-two scaling
+    ref = O.f32_to_bf16_bits_rne((xq.astype(np.float32) * sxs[:, None]).astype(np.float32))
+    assert np.array_equal(bf16_dev_to_bits(y), ref)

@@ -325,6 +325,23 @@ wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const
   uint8_t* sb = static_cast<uint8_t*>(scratch);
   int8_t* xq = reinterpret_cast<int8_t*>(sb);
   float* sx = reinterpret_cast<float*>(sb + al256(static_cast<size_t>(M) * K * 2));
+  if (decode2_supported(M, N, K, 4, c.sm_count)) {
+    // few tokens: the decode kernel quantizes the activations per token in
+    // its staging (same arithmetic as act_quant_int8), no separate pass
+    GemvArgs a{};
+    a.mode = GemvMode::kW4a8;
+    a.x = x;
+    a.packed = Wpacked4;
+    a.scales = scales;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.bits = 4;
+    a.y = y;
+    cudaError_t e = launch_decode2(c, a);
+    if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "w4a8_gemm launch");
+    return WQ_OK;
+  }
   if (use_prefill(M, N, K, 4)) {
     // many tokens: codes as exact bf16 values into the tensor-core GEMM,
     // which applies sx per output row

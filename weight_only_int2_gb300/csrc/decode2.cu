@@ -5,7 +5,8 @@
 // "Qwen3.8-27B-INT6-Mixed-AutoRound", section "Findings" (dense LSB-first
 // layout, symmetric 2^(b-1) zero point, bf16 group-128 scales of any sign);
 // "vLLM Quantization", section "Key points" (decode waits on memory); W4A8
-// per "int8 activations (W4A8) ...", section "Under the hood".
+// per "int8 activations (W4A8) ...", section "Under the hood" (the per-token
+// int8 quantization of the activations is done here, in the staging).
 //
 // Design (GB300):
 //  * Clusters of two CTAs, one CTA per SM. The output rows are cut into
@@ -49,9 +50,7 @@ constexpr int kXBatch = 3;                       // activation jobs a warp loads
 constexpr size_t kSmemCap = 227 * 1024 - 1024;   // dynamic smem budget (alignment slack)
 
 struct D2Params {
-  const uint16_t* x;   // bf16 [M, K] (WNA16)
-  const int8_t* xq;    // int8 [M, K] (W4A8)
-  const float* sx;     // [M] (W4A8)
+  const uint16_t* x;   // bf16 [M, K]
   int64_t M, N, K;
   int G, Gh;           // groups, groups per K half
   int C;               // clusters
@@ -121,26 +120,15 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// The 32 activations of a staged job, from their raw bf16 or int8 words.
-template <bool kInt8>
+// The 32 activations of a staged job, from their raw bf16 words.
 __device__ __forceinline__ void raw_to_float(const uint4 (&r)[4], float (&v)[32]) {
-  if constexpr (!kInt8) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t wv[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t wv[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        v[8 * c + 2 * e] = __uint_as_float(wv[e] << 16);
-        v[8 * c + 2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const uint32_t wv[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        v[16 * c + e] = static_cast<float>(static_cast<int8_t>((wv[e >> 2] >> (8 * (e & 3))) & 0xFFu));
+    for (int e = 0; e < 4; ++e) {
+      v[8 * c + 2 * e] = __uint_as_float(wv[e] << 16);
+      v[8 * c + 2 * e + 1] = __uint_as_float(wv[e] & 0xFFFF0000u);
     }
   }
 }
@@ -180,7 +168,7 @@ __host__ __device__ inline D2Smem d2_smem(int B, int NT, int T, int Gh, int sbox
   return s;
 }
 
-template <int B, int NT, bool kInt8>
+template <int B, int NT, bool kQuant>
 __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const __grid_constant__ CUtensorMap smap,
                                                               const D2Params p) {
@@ -188,6 +176,11 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
   constexpr int kTok = NT * 8;  // token columns of the partial-sum buffer
   extern __shared__ uint8_t smem_raw[];
   __shared__ volatile int s_abort;
+  __shared__ float s_sx[16];       // W4A8: per-token activation scales
+  __shared__ float s_f[16];        // W4A8: 2^k, k = clamp(1 - exponent(sx), -126, 127)
+  __shared__ float s_sxn[16];      // W4A8: sx 2^k
+  __shared__ float s_rcp[16];      // W4A8: RN(1 / (sx 2^k))
+  __shared__ float s_wmax[kCWarps];  // W4A8: per-warp partial maxima
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int Gh = p.Gh, T = p.T, NS = p.NS, ksplit = p.ksplit, H = p.H;
@@ -278,6 +271,59 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
     // wait for it first (no-op without a programmatic predecessor). Each warp
     // issues the loads of up to kXBatch jobs before building any fragments.
     griddep_wait();
+    if constexpr (kQuant) {
+      // W4A8: per-token int8 quantization of the activations, here instead of
+      // a separate pass. Every CTA needs the scales of all tokens, whichever
+      // K half it owns: amax over the whole row, split over 16 / Mp warps per
+      // token (Mp = M rounded up to a power of two), then sx = amax / 127 by
+      // IEEE division, as the activation-quant kernel does.
+      const int mp = p.M <= 1 ? 1 : p.M <= 2 ? 2 : p.M <= 4 ? 4 : p.M <= 8 ? 8 : 16;
+      const int wpt = kCWarps / mp, tok = warp / wpt, part = warp % wpt;
+      const int nch = static_cast<int>(p.K / 8);  // 16-byte chunks of a row
+      float amax = 0.0f;
+      if (tok < p.M) {
+        const uint4* row = reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(tok) * p.K);
+        const int stride = wpt * 32;
+        for (int i0 = part * 32 + lane; i0 < nch; i0 += 4 * stride) {
+          uint4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int idx = i0 + u * stride;
+            v[u] = idx < nch ? row[idx] : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              amax = fmaxf(amax, fabsf(__uint_as_float(wv[e] << 16)));
+              amax = fmaxf(amax, fabsf(__uint_as_float(wv[e] & 0xFFFF0000u)));
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      if (lane == 0) s_wmax[warp] = amax;
+      consumer_sync();
+      if (threadIdx.x < p.M) {
+        float a = 0.0f;
+        for (int w = 0; w < wpt; ++w) a = fmaxf(a, s_wmax[threadIdx.x * wpt + w]);
+        const float sxv = __fdiv_rn(a, 127.0f);
+        // a power of two that brings sx into [1, 2): x / sx = (x 2^k) / (sx 2^k)
+        // and both scalings are exact (bar an x 2^k that underflows, whose
+        // quotient is below 2^-126 and quantizes to 0 either way)
+        int e = 0;
+        (void)frexpf(sxv, &e);
+        const int k = max(-126, min(127, 1 - e));
+        const float f = sxv > 0.0f ? __uint_as_float(static_cast<uint32_t>(127 + k) << 23) : 0.0f;
+        s_sx[threadIdx.x] = sxv;
+        s_f[threadIdx.x] = f;
+        s_sxn[threadIdx.x] = sxv * f;
+        s_rcp[threadIdx.x] = sxv > 0.0f ? __frcp_rn(sxv * f) : 0.0f;
+      }
+      consumer_sync();
+    }
     for (int j0 = warp; j0 < NT * Gh; j0 += kXBatch * kCWarps) {
       uint4 rawv[kXBatch][4];
 #pragma unroll
@@ -290,15 +336,9 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
 #pragma unroll
         for (int c = 0; c < 4; ++c) rawv[b][c] = make_uint4(0u, 0u, 0u, 0u);
         if (valid) {
-          if constexpr (kInt8) {
-            const uint4* src = reinterpret_cast<const uint4*>(p.xq + tok * p.K + k0);
-            rawv[b][0] = src[0];
-            rawv[b][1] = src[1];
-          } else {
-            const uint4* src = reinterpret_cast<const uint4*>(p.x + tok * p.K + k0);
+          const uint4* src = reinterpret_cast<const uint4*>(p.x + tok * p.K + k0);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) rawv[b][c] = src[c];
-          }
+          for (int c = 0; c < 4; ++c) rawv[b][c] = src[c];
         }
       }
 #pragma unroll
@@ -307,7 +347,31 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
         if (job >= NT * Gh) break;  // warp-uniform
         const int gl = job % Gh, j = job / Gh;
         float xv[32];
-        raw_to_float<kInt8>(rawv[b], xv);
+        raw_to_float(rawv[b], xv);
+        if constexpr (kQuant) {
+          // xq = clamp(round_half_even(x / sx), -127, 127); an all-zero row
+          // (sx = 0) quantizes to zeros. The codes are exact in bf16.
+          const int64_t tok = j * 8 + g;
+          const bool live = tok < p.M;
+          const float f = live ? s_f[tok] : 0.0f;
+          const float sxn = live ? s_sxn[tok] : 0.0f;
+          const float rcp = live ? s_rcp[tok] : 0.0f;
+          // RN(x / sx) = RN(x' / sx') with x' = x 2^k, sx' = sx 2^k in [1, 2),
+          // by Markstein's correction of the product with y = RN(1 / sx'):
+          // q0 = RN(x' y), r = x' - q0 sx' exactly (fma), RN(q0 + r y) is the
+          // correctly rounded quotient (IBM J. Res. Dev. 34(1), 1990). With
+          // sx' in [2^-22, 2) (below 1 only for a subnormal sx, where k stops
+          // at 127) and |x'| <= 256 nothing overflows, and an underflowing
+          // quotient rounds to 0 as the exact one does. sx = 0 gives f = 0
+          // and zeros throughout.
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float xs = xv[c] * f;
+            const float q0 = xs * rcp;
+            const float r = fmaf(-q0, sxn, xs);
+            xv[c] = static_cast<float>(max(-127, min(127, __float2int_rn(fmaf(r, rcp, q0)))));
+          }
+        }
         uint32_t frag[16];
         float cr, sb;
         make_fragments<B>(xv, frag, cr, sb);
@@ -453,7 +517,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           const int64_t row = rc + rl;
           if (tok < p.M && row < r1) {
             float v = part[rl * kTok + tok] + inbox[rr * kTok + tok];
-            if constexpr (kInt8) v *= p.sx[tok];
+            if constexpr (kQuant) v *= s_sx[tok];
             p.y[tok * p.N + row] = float_to_bf16_bits_rn(v);
           }
         }
@@ -523,11 +587,11 @@ D2Plan make_d2plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
   return pl;
 }
 
-template <int B, int NT, bool kInt8>
+template <int B, int NT, bool kQuant>
 cudaError_t d2launch(const Ctx& c, const CUtensorMap& wmap, const CUtensorMap& smap, const D2Plan& pl) {
   static int configured[64] = {};  // dynamic smem opted in so far, per device
   if (c.device < 0 || c.device >= 64) return cudaErrorInvalidDevice;
-  auto kern = decode2_kernel<B, NT, kInt8>;
+  auto kern = decode2_kernel<B, NT, kQuant>;
   if (configured[c.device] < static_cast<int>(pl.smem)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
     if (e != cudaSuccess) return e;
@@ -552,9 +616,9 @@ cudaError_t d2launch(const Ctx& c, const CUtensorMap& wmap, const CUtensorMap& s
   return cudaLaunchKernelEx(&cfg, kern, wmap, smap, pl.prm);
 }
 
-template <bool kInt8>
+template <bool kQuant>
 cudaError_t d2launch_b(const Ctx& c, int bits, const CUtensorMap& wmap, const CUtensorMap& smap, const D2Plan& pl) {
-  if constexpr (kInt8) {
+  if constexpr (kQuant) {
     if (bits != 4) return cudaErrorInvalidValue;
     return pl.NT == 1 ? d2launch<4, 1, true>(c, wmap, smap, pl) : d2launch<4, 2, true>(c, wmap, smap, pl);
   } else {
@@ -583,14 +647,13 @@ bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count) 
 bool decode2_shape(int64_t M, int64_t K) { return M >= 1 && M <= 16 && K >= 1024 && K % 1024 == 0; }
 
 cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a) {
-  const bool int8 = a.mode == GemvMode::kW4a8;
-  if (a.mode != GemvMode::kWna16 && !int8) return cudaErrorInvalidValue;
+  // kW4a8 here: a.x is the bf16 activation, quantized per token in the kernel
+  const bool quant = a.mode == GemvMode::kW4a8;
+  if (a.mode != GemvMode::kWna16 && !quant) return cudaErrorInvalidValue;
   const D2Plan pl = make_d2plan(a.M, a.N, a.K, a.bits, c.sm_count);
   if (!pl.ok) return cudaErrorInvalidValue;
   D2Plan q = pl;
   q.prm.x = a.x;
-  q.prm.xq = a.xq;
-  q.prm.sx = a.sx;
   q.prm.y = a.y;
   q.prm.status = c.status;
   CUtensorMap wmap, smap;
@@ -601,7 +664,7 @@ cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a) {
   if (!make_tmap_bf16_2d(&smap, a.scales, static_cast<uint64_t>(pl.prm.G), static_cast<uint64_t>(a.N),
                          static_cast<uint32_t>(pl.prm.sbox), static_cast<uint32_t>(pl.prm.H)))
     return cudaErrorInvalidValue;
-  return int8 ? d2launch_b<true>(c, a.bits, wmap, smap, q) : d2launch_b<false>(c, a.bits, wmap, smap, q);
+  return quant ? d2launch_b<true>(c, a.bits, wmap, smap, q) : d2launch_b<false>(c, a.bits, wmap, smap, q);
 }
 
 }  // namespace wq

@@ -96,16 +96,17 @@ inline bool use_prefill(int64_t M, int64_t N, int64_t K, int bits) {
 }
 
 // Decode by CTA pairs (M <= 16, K % 1024 == 0): no workspace, no grid-wide
-// synchronisation. Modes kWna16 and kW4a8.
+// synchronisation. Mode kWna16 (bf16 x), or kW4a8 with a.x the bf16
+// activations, which the kernel quantizes per token itself.
 bool decode2_shape(int64_t M, int64_t K);
 bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count);
 cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a);
 
-// Routes a weight-streaming GEMM (few tokens): the CTA-pair decode kernel
-// when it applies, else the persistent split-K decode kernel, else the
-// chunked kernel.
+// Routes a weight-streaming GEMM (few tokens): WNA16 to the CTA-pair decode
+// kernel when it applies; otherwise (and W4A8 with precomputed int8 codes) the
+// persistent split-K decode kernel, else the chunked kernel.
 inline cudaError_t launch_stream_gemm(const Ctx& c, const GemvArgs& a) {
-  if (a.mode != GemvMode::kW4a8GroupAcc && decode2_supported(a.M, a.N, a.K, a.bits, c.sm_count))
+  if (a.mode == GemvMode::kWna16 && decode2_supported(a.M, a.N, a.K, a.bits, c.sm_count))
     return launch_decode2(c, a);
   return decode_supported(a.M, a.N, a.K, a.bits, c.sm_count) ? launch_decode(c, a) : launch_gemv(c, a);
 }
