@@ -80,9 +80,13 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+// The cluster barrier in two halves: every thread arrives once, early (after
+// its CTA's mbarriers exist), and waits only before its first access to the
+// peer's shared memory.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
@@ -135,6 +139,13 @@ __device__ __forceinline__ void raw_to_float(const uint4 (&r)[4], float (&v)[32]
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory");
 }
+// Named barrier 2 (all threads): the producer warp arrives once the
+// mbarriers are initialised, without waiting; the consumers wait on it
+// before their first mbarrier operation.
+__device__ __forceinline__ void init_done_arrive() {
+  asm volatile("bar.arrive 2, %0;" ::"n"(kThreads2) : "memory");
+}
+__device__ __forceinline__ void init_done_wait() { asm volatile("bar.sync 2, %0;" ::"n"(kThreads2) : "memory"); }
 
 template <int B>
 __device__ __forceinline__ void unpack_quad2(const uint32_t (&w)[B], int i2, uint32_t (&r)[4]) {
@@ -211,27 +222,31 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
   const uint32_t stage_bytes = static_cast<uint32_t>(H) * 16u * B;
   const uint32_t scale_bytes = static_cast<uint32_t>(H) * p.sbox * 2u;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], T);  // the T warps (one per tile) that read a stage
-    }
-    mbar_init(&cdone[0], kCWarps);
-    mbar_init(&cdone[1], kCWarps);
-    mbar_init(rbar, 1);
-    mbar_init(dbar, 1);
-    mbar_init(&sfull[0], 1);
-    mbar_init(&sfull[1], 1);
-    s_abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  cluster_sync_all();  // the peer's barriers exist before anything arrives on them
   if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp == kCWarps) {
-    // ---- producer: chunk k = rows r0 + k H .. + H - 1; stage = one group of
-    // this CTA's K half; the chunk's first stage also brings its scale box
+    // ---- producer: initialise the barriers, then stream at once; the
+    // consumers learn of the initialisation through named barrier 2, the
+    // peer CTA through the cluster barrier
+    if (lane == 0) {
+      for (int s = 0; s < NS; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], T);  // the T warps (one per tile) that read a stage
+      }
+      mbar_init(&cdone[0], kCWarps);
+      mbar_init(&cdone[1], kCWarps);
+      mbar_init(rbar, 1);
+      mbar_init(dbar, 1);
+      mbar_init(&sfull[0], 1);
+      mbar_init(&sfull[1], 1);
+      s_abort = 0;
+      fence_mbar_init();
+    }
+    __syncwarp();
+    cluster_arrive();
+    init_done_arrive();
+    // chunk k = rows r0 + k H .. + H - 1; stage = one group of this CTA's K
+    // half; the chunk's first stage also brings its scale box
     if (lane == 0) {
       uint32_t it = 0;
       bool stop = false;
@@ -260,8 +275,10 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
       }
     }
     __syncwarp();
+    cluster_wait();
   } else {
     // ---- consumers
+    cluster_arrive();
     const bool active = warp < T * ksplit;
     const int tile = warp % T, kr = warp / T;
     const int g = lane >> 2, t = lane & 3;
@@ -271,6 +288,26 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
     // wait for it first (no-op without a programmatic predecessor). Each warp
     // issues the loads of up to kXBatch jobs before building any fragments.
     griddep_wait();
+    uint4 rawv[kXBatch][4];
+    auto load_x_batch = [&](int j0, uint4 (&dst)[kXBatch][4]) {
+#pragma unroll
+      for (int b = 0; b < kXBatch; ++b) {
+        const int job = j0 + b * kCWarps;
+        const int gl = job % Gh, j = job / Gh;
+        const int64_t tok = j * 8 + g;
+        const bool valid = job < NT * Gh && tok < p.M;
+        const int64_t k0 = static_cast<int64_t>(gbase + gl) * 128 + 32 * t;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[b][c] = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.x + tok * p.K + k0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) dst[b][c] = src[c];
+        }
+      }
+    };
+    // W4A8: the first batch is in flight during the amax pass below
+    if constexpr (kQuant) load_x_batch(warp, rawv);
     if constexpr (kQuant) {
       // W4A8: per-token int8 quantization of the activations, here instead of
       // a separate pass. Every CTA needs the scales of all tokens, whichever
@@ -325,22 +362,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
       consumer_sync();
     }
     for (int j0 = warp; j0 < NT * Gh; j0 += kXBatch * kCWarps) {
-      uint4 rawv[kXBatch][4];
-#pragma unroll
-      for (int b = 0; b < kXBatch; ++b) {
-        const int job = j0 + b * kCWarps;
-        const int gl = job % Gh, j = job / Gh;
-        const int64_t tok = j * 8 + g;
-        const bool valid = job < NT * Gh && tok < p.M;
-        const int64_t k0 = static_cast<int64_t>(gbase + gl) * 128 + 32 * t;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) rawv[b][c] = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) {
-          const uint4* src = reinterpret_cast<const uint4*>(p.x + tok * p.K + k0);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) rawv[b][c] = src[c];
-        }
-      }
+      if (!kQuant || j0 != warp) load_x_batch(j0, rawv);
 #pragma unroll
       for (int b = 0; b < kXBatch; ++b) {
         const int job = j0 + b * kCWarps;
@@ -386,6 +408,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
       }
     }
     consumer_sync();
+    init_done_wait();  // the producer has initialised the barriers
 
     bool stop = false;  // warp-uniform
     for (int k = 0; k < nck; ++k) {
@@ -490,6 +513,9 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
         }
         consumer_sync();
       }
+      // the peer's barriers exist (it arrived on the cluster barrier after
+      // initialising them) before anything of ours reaches its memory
+      if (k == 0) cluster_wait();
       // push our sums of the rows the peer finalises into its inbox (remote
       // 16-byte stores, no waiting), then tell it they are there
       const int half_rows = T * (kTileRows / 2);
