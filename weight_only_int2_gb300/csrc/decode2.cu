@@ -147,6 +147,32 @@ __device__ __forceinline__ void init_done_arrive() {
 }
 __device__ __forceinline__ void init_done_wait() { asm volatile("bar.sync 2, %0;" ::"n"(kThreads2) : "memory"); }
 
+// m16n8k16 MMA with f32 accumulators, D = A B + C (kZero: C = 0). Not
+// volatile: the compiler may schedule it like any other arithmetic.
+template <bool kF16, bool kZero>
+__device__ __forceinline__ void mma16c(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                       uint32_t b1) {
+  if constexpr (kZero) {
+    if constexpr (kF16)
+      asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+          : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+    else
+      asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+          : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+  } else {
+    if constexpr (kF16)
+      asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+      asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
 template <int B>
 __device__ __forceinline__ void unpack_quad2(const uint32_t (&w)[B], int i2, uint32_t (&r)[4]) {
   constexpr uint32_t kMagic = uses_fp16<B>() ? 0x64006400u : 0x43004300u;
@@ -411,6 +437,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
     init_done_wait();  // the producer has initialised the barriers
 
     bool stop = false;  // warp-uniform
+    uint32_t slot_cur = static_cast<uint32_t>(kr), phase_cur = 0;  // this warp's next stage: slot, phase
     for (int k = 0; k < nck; ++k) {
       const int64_t rc = r0 + static_cast<int64_t>(k) * H;
       const uint16_t* sbk = sbuf + (k & 1) * sbox_elems;
@@ -431,8 +458,16 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
       if (active && !stop) {
         const int rowt = tile * kTileRows + g;  // rows rowt + {0, 8, 16, 24} of the chunk
         for (int gl = kr; gl < Gh; gl += ksplit) {
-          const uint32_t it = static_cast<uint32_t>(k) * Gh + gl, s = it % NS;
-          if (!__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&full[s], (it / NS) & 1))) {
+          // stage it = k Gh + gl sits in slot it % NS, phase it / NS; a warp's
+          // stages advance by ksplit, which divides NS and Gh, so both are
+          // carried along instead of divided out
+          const uint32_t s = slot_cur, phase = phase_cur;
+          slot_cur += static_cast<uint32_t>(ksplit);
+          if (slot_cur >= static_cast<uint32_t>(NS)) {
+            slot_cur -= static_cast<uint32_t>(NS);
+            phase_cur ^= 1u;
+          }
+          if (!__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&full[s], phase))) {
             if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
             s_abort = 1;
             stop = true;
@@ -452,12 +487,6 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           for (int qq = 0; qq < 4; ++qq) sc[qq] = bf16_bits_to_float(sbk[(rowt + 8 * qq) * p.sbox + scol]);
           float c[NT][2][4];
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) c[j][h][e] = 0.0f;
-#pragma unroll
           for (int i2 = 0; i2 < 4; ++i2) {
             uint32_t a0[4], a1[4], a2[4], a3[4];
             unpack_quad2<B>(w0, i2, a0);
@@ -467,10 +496,15 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
               const uint4 bv = xs4[((j * Gh + gl) * 4 + i2) * 32 + lane];
-              mma16<kF16>(c[j][0], a0[0], a1[0], a0[1], a1[1], bv.x, bv.y);
-              mma16<kF16>(c[j][1], a2[0], a3[0], a2[1], a3[1], bv.x, bv.y);
-              mma16<kF16>(c[j][0], a0[2], a1[2], a0[3], a1[3], bv.z, bv.w);
-              mma16<kF16>(c[j][1], a2[2], a3[2], a2[3], a3[3], bv.z, bv.w);
+              if (i2 == 0) {  // the group's chains start from zero
+                mma16c<kF16, true>(c[j][0], a0[0], a1[0], a0[1], a1[1], bv.x, bv.y);
+                mma16c<kF16, true>(c[j][1], a2[0], a3[0], a2[1], a3[1], bv.x, bv.y);
+              } else {
+                mma16c<kF16, false>(c[j][0], a0[0], a1[0], a0[1], a1[1], bv.x, bv.y);
+                mma16c<kF16, false>(c[j][1], a2[0], a3[0], a2[1], a3[1], bv.x, bv.y);
+              }
+              mma16c<kF16, false>(c[j][0], a0[2], a1[2], a0[3], a1[3], bv.z, bv.w);
+              mma16c<kF16, false>(c[j][1], a2[2], a3[2], a2[3], a3[3], bv.z, bv.w);
             }
           }
 #pragma unroll
