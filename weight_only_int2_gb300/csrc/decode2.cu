@@ -45,7 +45,7 @@ constexpr int kCWarps = 16;                      // consumer warps
 constexpr int kThreads2 = (kCWarps + 1) * 32;    // + one producer warp
 constexpr int kTileRows = 32;                    // rows per warp tile
 constexpr int kMaxH = 256;                       // rows per chunk (TMA box limit)
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 24;                   // ring slots at most (a small layer streams whole)
 constexpr int kXBatch = 3;                       // activation jobs a warp loads at once
 constexpr size_t kSmemCap = 227 * 1024 - 1024;   // dynamic smem budget (alignment slack)
 
@@ -185,17 +185,22 @@ __device__ __forceinline__ void unpack_quad2(const uint32_t (&w)[B], int i2, uin
   }
 }
 
-// Shared-memory carve-up, identical on host (planning) and device.
+// Shared-memory carve-up, identical on host (planning) and device. A ring
+// slot and a scale buffer hold the H rows their TMA box brings; the warps of
+// the last tile also read the rows up to T * 32 - 1 past them (bytes of the
+// next region, whose results are never written), which stay inside the
+// allocation since the scale buffers and the fragments follow the ring.
 struct D2Smem {
-  size_t ring, slot, sbuf, xs, corr, scl, part, inbox, bars, total;
+  size_t ring, slot, sbuf, shalf, xs, corr, scl, part, inbox, bars, total;
 };
-__host__ __device__ inline D2Smem d2_smem(int B, int NT, int T, int Gh, int sbox, int NS) {
+__host__ __device__ inline D2Smem d2_smem(int B, int NT, int T, int H, int Gh, int sbox, int NS) {
   D2Smem s{};
   auto al = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
-  s.slot = al(static_cast<size_t>(T) * kTileRows * 16 * B, 1024);
+  s.slot = al(static_cast<size_t>(H) * 16 * B, 128);
   s.ring = 0;
   s.sbuf = s.ring + NS * s.slot;
-  s.xs = al(s.sbuf + 2 * static_cast<size_t>(T) * kTileRows * sbox * 2, 128);
+  s.shalf = al(static_cast<size_t>(H) * sbox * 2, 128);  // one of the two scale buffers
+  s.xs = al(s.sbuf + 2 * s.shalf, 128);
   s.corr = s.xs + static_cast<size_t>(NT) * Gh * 4 * 32 * 16;
   s.scl = s.corr + static_cast<size_t>(NT) * 8 * Gh * 4;
   s.part = al(s.scl + static_cast<size_t>(NT) * 8 * Gh * 4, 16);
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int Gh = p.Gh, T = p.T, NS = p.NS, ksplit = p.ksplit, H = p.H;
-  const D2Smem L = d2_smem(B, NT, T, Gh, p.sbox, NS);
+  const D2Smem L = d2_smem(B, NT, T, H, Gh, p.sbox, NS);
   uint8_t* ring = base + L.ring;
   uint16_t* sbuf = reinterpret_cast<uint16_t*>(base + L.sbuf);
   uint4* xs4 = reinterpret_cast<uint4*>(base + L.xs);
@@ -244,7 +249,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
   const int nck = static_cast<int>((r1 - r0 + H - 1) / H);      // chunks (the same in both CTAs)
   const int gbase = static_cast<int>(q) * Gh;                    // first group of this half
   const int scol0 = static_cast<int>(q) * p.sx0;                 // scale box start column
-  const int sbox_elems = T * kTileRows * p.sbox;
+  const int sbox_elems = static_cast<int>(L.shalf / 2);  // elements between the two scale buffers
   const uint32_t stage_bytes = static_cast<uint32_t>(H) * 16u * B;
   const uint32_t scale_bytes = static_cast<uint32_t>(H) * p.sbox * 2u;
 
@@ -575,7 +580,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           const int rr = e % half_rows, tok = e / half_rows;
           const int rl = static_cast<int>(q) * half_rows + rr;
           const int64_t row = rc + rl;
-          if (tok < p.M && row < r1) {
+          if (tok < p.M && rl < H && row < r1) {  // tile rows past H are not the chunk's
             float v = part[rl * kTok + tok] + inbox[rr * kTok + tok];
             if constexpr (kQuant) v *= s_sx[tok];
             p.y[tok * p.N + row] = float_to_bf16_bits_rn(v);
@@ -634,7 +639,7 @@ D2Plan make_d2plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
   for (int ks = kCWarps / p.T; ks >= 1 && p.NS == 0; --ks) {
     if (ks > p.Gh || p.Gh % ks != 0) continue;
     for (int ns = (kMaxStages / ks) * ks; ns >= ks && ns >= 2; ns -= ks) {
-      if (d2_smem(bits, pl.NT, p.T, p.Gh, p.sbox, ns).total <= kSmemCap) {
+      if (d2_smem(bits, pl.NT, p.T, p.H, p.Gh, p.sbox, ns).total <= kSmemCap) {
         p.ksplit = ks;
         p.NS = ns;
         break;
@@ -642,7 +647,7 @@ D2Plan make_d2plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
     }
   }
   if (p.NS < 2 || p.ksplit < 1) return pl;
-  pl.smem = d2_smem(bits, pl.NT, p.T, p.Gh, p.sbox, p.NS).total + 1024;  // + base alignment
+  pl.smem = d2_smem(bits, pl.NT, p.T, p.H, p.Gh, p.sbox, p.NS).total + 1024;  // + base alignment
   pl.ok = true;
   return pl;
 }
