@@ -432,6 +432,36 @@ def _time_extras(wq, torch, stream):
     return out
 
 
+def run_prefill_case(args):
+    """One prefill shape on its own (bits, M; N = 17408, K = 5120): a small,
+    self-contained workload for profiling the tensor-core kernel."""
+    import torch
+
+    import weight_only_int2_gb300 as wq
+    from weight_only_int2_gb300 import _build
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    _build.build()
+    wq.load()
+    bits, M = args.prefill_case
+    N, K = 17408, K_DIM
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(4321)
+    packed, s = _rand_layer(wq, torch, N, K, bits, gen)
+    x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            wq.wna16_gemm(x, packed, s, N, K, bits, y=y)
+    ms = _event_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, N, K, bits, y=y), args.steps)
+    wq.check_status()
+    _, bf16, _, src = _peaks()
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    print(json.dumps({"prefill_case": {"bits": bits, "M": M, "N": N, "K": K}, "ms": round(ms, 4),
+                      "TFLOPS": round(tf, 1), "frac": round(tf / bf16, 4), "peak_source": src}), flush=True)
+
+
 # ----------------------------------------------------------------------------- oracle arms
 
 def _cpu_time_oracle(budget_s: float):
@@ -501,13 +531,25 @@ def main():
                     help="skip the other rows (prefill, W4A8, lm_head, gather, stack)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--prefill-case", type=str, default=None,
+                    help="time one prefill shape 'bits,M' (N=17408, K=5120) alone (profiling)")
     ap.add_argument("--case", type=str, default=None,
                     help="restrict the decode sweep to one case 'bits,N,M' (profiling)")
     args = ap.parse_args()
     if args.case is not None:
         args.case = tuple(int(v) for v in args.case.split(","))
+        if (len(args.case) != 3 or args.case[0] not in DECODE_BITS or args.case[1] not in DECODE_N
+                or args.case[2] not in DECODE_M):
+            ap.error(f"--case must name a case of the sweep: bits in {DECODE_BITS}, N in {DECODE_N}, "
+                     f"M in {DECODE_M}")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.prefill_case is not None:
+        args.prefill_case = tuple(int(v) for v in args.prefill_case.split(","))
+        if len(args.prefill_case) != 2 or not 2 <= args.prefill_case[0] <= 8 or args.prefill_case[1] < 1:
+            ap.error("--prefill-case wants 'bits,M' with bits in 2..8")
+        run_prefill_case(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
