@@ -315,30 +315,47 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
     const int g = lane >> 2, t = lane & 3;
 
     // activation fragments of this K half, built once while the producer
-    // streams weights. The activations are the previous kernel's output:
-    // wait for it first (no-op without a programmatic predecessor). Each warp
-    // issues the loads of up to kXBatch jobs before building any fragments.
+    // streams weights. A task is one (token, group) of the half: the four
+    // lanes t = 0..3 of a lane quad take its 128 activations, eight tasks per
+    // warp pass, so that a few tokens still fill whole warps. The fragments
+    // and corrections of the token columns past M are zero (scale 1); they
+    // are written first, since they do not wait for the previous kernel,
+    // whose output the activations are.
+    const int ntask = static_cast<int>(p.M) * Gh;
+    const int nwt = (ntask + 7) / 8;  // warp tasks: eight tasks each
+    {
+      const int zt0 = static_cast<int>(p.M), nz = NT * 8 - zt0;
+      for (int e = threadIdx.x; e < nz * Gh * 16; e += kCWarps * 32) {
+        const int tk = zt0 + e / (Gh * 16), rem = e % (Gh * 16);
+        const int gz = rem >> 4, i2 = (rem >> 2) & 3, tt = rem & 3;
+        xs4[(((tk >> 3) * Gh + gz) * 4 + i2) * 32 + (tk & 7) * 4 + tt] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      for (int e = threadIdx.x; e < nz * Gh; e += kCWarps * 32) {
+        corr[zt0 * Gh + e] = 0.0f;
+        scl[zt0 * Gh + e] = 1.0f;
+      }
+    }
     griddep_wait();
+    // Each warp issues the loads of up to kXBatch of its passes (warp task
+    // q * kCWarps + warp for its q-th pass) before building any fragments.
     uint4 rawv[kXBatch][4];
-    auto load_x_batch = [&](int j0, uint4 (&dst)[kXBatch][4]) {
+    auto load_x_batch = [&](int q0, uint4 (&dst)[kXBatch][4]) {
 #pragma unroll
       for (int b = 0; b < kXBatch; ++b) {
-        const int job = j0 + b * kCWarps;
-        const int gl = job % Gh, j = job / Gh;
-        const int64_t tok = j * 8 + g;
-        const bool valid = job < NT * Gh && tok < p.M;
-        const int64_t k0 = static_cast<int64_t>(gbase + gl) * 128 + 32 * t;
+        const int task = ((q0 + b) * kCWarps + warp) * 8 + g;
 #pragma unroll
         for (int c = 0; c < 4; ++c) dst[b][c] = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) {
-          const uint4* src = reinterpret_cast<const uint4*>(p.x + tok * p.K + k0);
+        if (task < ntask) {
+          const int tok = task / Gh, gl = task % Gh;
+          const int64_t k0 = static_cast<int64_t>(gbase + gl) * 128 + 32 * t;
+          const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(tok) * p.K + k0);
 #pragma unroll
           for (int c = 0; c < 4; ++c) dst[b][c] = src[c];
         }
       }
     };
     // W4A8: the first batch is in flight during the amax pass below
-    if constexpr (kQuant) load_x_batch(warp, rawv);
+    if constexpr (kQuant) load_x_batch(0, rawv);
     if constexpr (kQuant) {
       // W4A8: per-token int8 quantization of the activations, here instead of
       // a separate pass. Every CTA needs the scales of all tokens, whichever
@@ -392,23 +409,23 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
       }
       consumer_sync();
     }
-    for (int j0 = warp; j0 < NT * Gh; j0 += kXBatch * kCWarps) {
-      if (!kQuant || j0 != warp) load_x_batch(j0, rawv);
+    for (int q0 = 0; q0 * kCWarps + warp < nwt; q0 += kXBatch) {  // warp-uniform
+      if (!kQuant || q0 != 0) load_x_batch(q0, rawv);
 #pragma unroll
       for (int b = 0; b < kXBatch; ++b) {
-        const int job = j0 + b * kCWarps;
-        if (job >= NT * Gh) break;  // warp-uniform
-        const int gl = job % Gh, j = job / Gh;
+        const int wt = (q0 + b) * kCWarps + warp;
+        if (wt >= nwt) break;  // warp-uniform
+        const int task = wt * 8 + g;
+        const bool valid = task < ntask;  // lane quads past the last task build zeros
+        const int tok = valid ? task / Gh : 0, gl = valid ? task % Gh : 0;
         float xv[32];
         raw_to_float(rawv[b], xv);
         if constexpr (kQuant) {
           // xq = clamp(round_half_even(x / sx), -127, 127); an all-zero row
           // (sx = 0) quantizes to zeros. The codes are exact in bf16.
-          const int64_t tok = j * 8 + g;
-          const bool live = tok < p.M;
-          const float f = live ? s_f[tok] : 0.0f;
-          const float sxn = live ? s_sxn[tok] : 0.0f;
-          const float rcp = live ? s_rcp[tok] : 0.0f;
+          const float f = valid ? s_f[tok] : 0.0f;
+          const float sxn = valid ? s_sxn[tok] : 0.0f;
+          const float rcp = valid ? s_rcp[tok] : 0.0f;
           // RN(x / sx) = RN(x' / sx') with x' = x 2^k, sx' = sx 2^k in [1, 2),
           // by Markstein's correction of the product with y = RN(1 / sx'):
           // q0 = RN(x' y), r = x' - q0 sx' exactly (fma), RN(q0 + r y) is the
@@ -427,14 +444,16 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
         }
         uint32_t frag[16];
         float cr, sb;
-        make_fragments<B>(xv, frag, cr, sb);
+        make_fragments<B>(xv, frag, cr, sb);  // every lane: it shuffles within its quad
+        if (valid) {
 #pragma unroll
-        for (int i2 = 0; i2 < 4; ++i2)
-          xs4[((j * Gh + gl) * 4 + i2) * 32 + lane] =
-              make_uint4(frag[4 * i2], frag[4 * i2 + 1], frag[4 * i2 + 2], frag[4 * i2 + 3]);
-        if (t == 0) {
-          corr[(j * 8 + g) * Gh + gl] = cr;
-          scl[(j * 8 + g) * Gh + gl] = sb;
+          for (int i2 = 0; i2 < 4; ++i2)
+            xs4[(((tok >> 3) * Gh + gl) * 4 + i2) * 32 + (tok & 7) * 4 + t] =
+                make_uint4(frag[4 * i2], frag[4 * i2 + 1], frag[4 * i2 + 2], frag[4 * i2 + 3]);
+          if (t == 0) {
+            corr[tok * Gh + gl] = cr;
+            scl[tok * Gh + gl] = sb;
+          }
         }
       }
     }
