@@ -139,8 +139,9 @@ size_t w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K);
  * undefined. */
 size_t w4a8_scratch_bytes(int64_t M, int64_t K);
 
-/* W4A8 linear layer [W4A8]: act_quant_int8(x) into `scratch`, then with int4
- * codes q and zero point 8,
+/* W4A8 linear layer [W4A8]: act_quant_int8(x) (into `scratch`; for M <= 16
+ * and K % 1024 == 0 inside the decode kernel, same arithmetic), then with
+ * int4 codes q and zero point 8,
  *   acc[m, n, g] = sum_{k in group g} xq[m, k] * (q[n, k] - 8)   (exact, int32)
  *   y[m, n] = bf16( sx[m] * sum_g s[n, g] * acc[m, n, g] ).
  *  Wpacked4 [N, K/8] uint32 (v1 layout, bits = 4); scales [N, K/128] bf16.

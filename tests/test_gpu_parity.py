@@ -213,6 +213,23 @@ def test_gather_bit_exact(bits):
     assert np.all(bf16_dev_to_bits(out)[0, :128] == 0x8000)
 
 
+@pytest.mark.parametrize("bits", [5, 8])
+def test_gather_long_rows(bits):
+    """Rows longer than any shared-memory staging could hold (256 K codes,
+    up to 256 KB packed): the gather reads them from global memory."""
+    V, D, T = 5, 262144, 7
+    q = I.make_codes(V, D, bits, 90 + bits)
+    s = I.make_scales(V, D // 128, 91)
+    ids = np.array([4, 0, 2, 2, -1, 3, 1], dtype=np.int32)
+    packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(s), bits)
+    bad = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = wq.qembed_gather(to_dev(ids), packed, s_dev, V, D, bits, bad_count=bad)
+    torch.cuda.synchronize()
+    ref, nbad = O.qembed_ref(ids, q, s, bits)
+    assert np.array_equal(bf16_dev_to_bits(out), ref)
+    assert int(bad.item()) == nbad == 1
+
+
 def test_gather_empty():
     packed, s_dev = wq.wna16_repack(to_dev(I.make_codes(4, 128, 8, 1)),
                                     to_dev_bf16(I.make_scales(4, 1, 2)), 8)

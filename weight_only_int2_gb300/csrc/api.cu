@@ -378,8 +378,6 @@ wq_status qembed_gather(const int32_t* ids, int64_t T, const uint32_t* Wpacked, 
   WQ_TRY(check_bits(bits));
   WQ_TRY(check_group_k(group, D, "D"));
   if (T < 0 || V < 1) return fail(WQ_EINVAL, "T must be >= 0 and V >= 1");
-  if (static_cast<int64_t>(D) * bits / 8 > 200 * 1024)
-    return fail(WQ_EUNSUPPORTED, "packed row of %lld bytes exceeds shared memory", (long long)(D * bits / 8));
   if (T == 0) return WQ_OK;
   WQ_PTR(ids);
   WQ_PTR(Wpacked);

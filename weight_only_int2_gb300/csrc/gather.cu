@@ -10,8 +10,11 @@
 // The float32 product is exact, so the single bf16 rounding matches the
 // definition; q == zero point with a negative scale yields -0.0.
 //
-// One CTA per token: one bulk copy (TMA engine) brings the packed row into
-// shared memory, then each thread expands 32-code slices into 64 output bytes.
+// One CTA per token. Thread u reads the b words of its 32-code slice u
+// straight from global memory (the warp's loads cover one contiguous span of
+// the row, in the widest loads the alignment of u * b words allows), expands
+// them and writes its 64 output bytes. No shared-memory staging and no
+// barrier: any row length works, and no wait can stall.
 #include "wq_device.cuh"
 #include "wq_internal.h"
 
@@ -20,13 +23,34 @@ namespace {
 
 constexpr int kThreads = 128;
 
+// Words u * B .. u * B + B - 1 of a row (the row starts 16-byte aligned).
+template <int B>
+__device__ __forceinline__ void load_slice_words(const uint32_t* __restrict__ row, int64_t u, uint32_t (&w)[B + 1]) {
+  const uint32_t* src = row + u * B;
+  if constexpr (B % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < B; i += 4) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + i));
+      w[i] = v.x, w[i + 1] = v.y, w[i + 2] = v.z, w[i + 3] = v.w;
+    }
+  } else if constexpr (B % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < B; i += 2) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(src + i));
+      w[i] = v.x, w[i + 1] = v.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < B; ++i) w[i] = __ldg(src + i);
+  }
+  w[B] = 0u;
+}
+
 template <int B>
 __global__ void __launch_bounds__(kThreads) gather_kernel(
     const int32_t* __restrict__ ids, const uint32_t* __restrict__ packed,
     const uint16_t* __restrict__ scales, int64_t V, int64_t D, uint16_t* __restrict__ out,
-    int32_t* __restrict__ bad_count, unsigned* __restrict__ status) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bar;
+    int32_t* __restrict__ bad_count) {
   const int64_t t = blockIdx.x;
   const int64_t id = ids[t];
   const int64_t units = D / 32;
@@ -41,29 +65,14 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(
     return;
   }
 
-  const uint32_t row_bytes = static_cast<uint32_t>(units * 4 * B);
-  if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(&bar, row_bytes);
-    bulk_load(smem, packed + id * units * B, row_bytes, &bar);
-  }
-  __syncthreads();
-  if (!mbar_wait_bounded(&bar, 0)) {
-    record_status(status, kStatusTimeout);
-    return;
-  }
-
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(smem);
+  const uint32_t* prow = packed + id * units * B;
   const uint16_t* srow = scales + id * (D / 128);
   constexpr uint32_t kMask = (1u << B) - 1u;
   constexpr int kZero = 1 << (B - 1);
   for (int64_t u = threadIdx.x; u < units; u += kThreads) {
     uint32_t win[B + 1];
-#pragma unroll
-    for (int i = 0; i < B; ++i) win[i] = w[u * B + i];
-    win[B] = 0u;
-    const float s = bf16_bits_to_float(srow[u >> 2]);
+    load_slice_words<B>(prow, u, win);
+    const float s = bf16_bits_to_float(__ldg(srow + (u >> 2)));
     uint32_t o[16];
 #pragma unroll
     for (int c = 0; c < 32; c += 2) {
@@ -87,14 +96,8 @@ template <int B>
 cudaError_t launch_b(const Ctx& c, const int32_t* ids, int64_t T, const uint32_t* packed,
                      const uint16_t* scales, int64_t V, int64_t D, uint16_t* out,
                      int32_t* bad_count) {
-  const size_t smem = static_cast<size_t>(D / 32) * 4 * B;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(gather_kernel<B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  gather_kernel<B><<<static_cast<unsigned>(T), kThreads, smem, c.stream>>>(
-      ids, packed, scales, V, D, out, bad_count, c.status);
+  gather_kernel<B><<<static_cast<unsigned>(T), kThreads, 0, c.stream>>>(ids, packed, scales, V, D, out,
+                                                                        bad_count);
   return cudaGetLastError();
 }
 
