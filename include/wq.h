@@ -167,6 +167,16 @@ wq_status qembed_gather(const int32_t* ids, int64_t T, const uint32_t* Wpacked,
 
 /* ---- test and debug entry points ---------------------------------------- */
 
+/* The launch plan of the CTA-pair decode kernel for a shape (host only, no
+ * device call), for checks of its invariants. out14 receives, in order:
+ * usable (1/0), clusters C, chunk rows H, chunks, 32-row tiles T, warps per
+ * tile ksplit, ring slots NS, groups G, groups per K half, scale-box width,
+ * scale-box start of the second half, token groups of 8, dynamic shared
+ * memory bytes, and the most ring slots the kernel supports. The entries
+ * after the first are meaningful only when it is 1. WQ_EINVAL for bits
+ * outside 2..8, sm_count < 1 or a NULL out14. */
+wq_status wq_debug_decode_plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count, int64_t* out14);
+
 /* Inverse of the repack for the codes: packed [N, ceil(K*bits/32)] ->
  * codes [N, K] uint8. */
 wq_status wq_debug_unpack(const uint32_t* packed, int64_t N, int64_t K, int bits,

@@ -9,6 +9,7 @@ from ._lib import (  # noqa: F401
     WQError,
     act_quant_int8,
     check_status,
+    debug_decode_plan,
     debug_unpack,
     debug_w4a8_group_acc,
     load,

@@ -40,6 +40,7 @@ SIGNATURES = {
                            _c_size, _c_ptr, _c_size, _c_ptr]),
     "qembed_gather": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_int, _c_int, _c_ptr,
                                _c_ptr, _c_ptr]),
+    "wq_debug_decode_plan": (_c_int, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_ptr]),
     "wq_debug_unpack": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr]),
     "wq_debug_w4a8_group_acc": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr]),
     "wq_check_status": (_c_int, []),
@@ -265,6 +266,17 @@ def qembed_gather(ids: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
     _check(load().qembed_gather(_ptr(ids), T, _ptr(packed), _ptr(scales), V, D, bits, group, _ptr(out),
                                 _ptr(bad_count), _stream()), "qembed_gather")
     return out
+
+
+_PLAN_KEYS = ("ok", "C", "H", "nchunk", "T", "ksplit", "NS", "G", "Gh", "sbox", "sx0", "NT", "smem",
+              "max_slots")
+
+
+def debug_decode_plan(M: int, N: int, K: int, bits: int, sm_count: int) -> dict:
+    """The CTA-pair decode kernel's launch plan for a shape (host only)."""
+    out = (ctypes.c_int64 * len(_PLAN_KEYS))()
+    _check(load().wq_debug_decode_plan(M, N, K, bits, sm_count, ctypes.addressof(out)), "wq_debug_decode_plan")
+    return dict(zip(_PLAN_KEYS, (int(v) for v in out)))
 
 
 def debug_unpack(packed: torch.Tensor, N: int, K: int, bits: int) -> torch.Tensor:

@@ -390,6 +390,14 @@ wq_status qembed_gather(const int32_t* ids, int64_t T, const uint32_t* Wpacked, 
   return WQ_OK;
 }
 
+wq_status wq_debug_decode_plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count, int64_t* out14) {
+  t_err[0] = 0;
+  WQ_PTR(out14);
+  if (bits < 2 || bits > 8 || sm_count < 1) return fail(WQ_EINVAL, "bits must be in 2..8 and sm_count >= 1");
+  decode2_plan_info(M, N, K, bits, sm_count, out14);
+  return WQ_OK;
+}
+
 wq_status wq_debug_unpack(const uint32_t* packed, int64_t N, int64_t K, int bits, uint8_t* codes,
                           void* stream) {
   t_err[0] = 0;

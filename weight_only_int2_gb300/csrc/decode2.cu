@@ -730,6 +730,15 @@ bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count) 
 
 bool decode2_shape(int64_t M, int64_t K) { return M >= 1 && M <= 16 && K >= 1024 && K % 1024 == 0; }
 
+int decode2_plan_info(int64_t M, int64_t N, int64_t K, int bits, int sm_count, int64_t* out) {
+  const D2Plan pl = make_d2plan(M, N, K, bits, sm_count);
+  const D2Params& p = pl.prm;
+  const int64_t v[14] = {pl.ok ? 1 : 0, p.C, p.H, p.nchunk, p.T, p.ksplit, p.NS, p.G, p.Gh,
+                         p.sbox, p.sx0, pl.NT, static_cast<int64_t>(pl.smem), kMaxStages};
+  for (int i = 0; i < 14; ++i) out[i] = v[i];
+  return pl.ok ? 1 : 0;
+}
+
 cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a) {
   // kW4a8 here: a.x is the bf16 activation, quantized per token in the kernel
   const bool quant = a.mode == GemvMode::kW4a8;

@@ -99,6 +99,9 @@ inline bool use_prefill(int64_t M, int64_t N, int64_t K, int bits) {
 // synchronisation. Mode kWna16 (bf16 x), or kW4a8 with a.x the bf16
 // activations, which the kernel quantizes per token itself.
 bool decode2_shape(int64_t M, int64_t K);
+// The CTA-pair decode plan for a shape, for host-side checks: out[14] =
+// {ok, C, H, nchunk, T, ksplit, NS, G, Gh, sbox, sx0, NT, smem bytes, max ring slots}.
+int decode2_plan_info(int64_t M, int64_t N, int64_t K, int bits, int sm_count, int64_t* out);
 bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count);
 cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a);
 
