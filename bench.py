@@ -369,6 +369,20 @@ def _time_extras(wq, torch, stream):
         del packed, s
     out["prefill"] = rows
 
+    # the decode configuration's M = 64 cases (outside the M <= 16 headline):
+    # the chunked streaming kernel, on packed-weight bytes
+    rows = []
+    for bits in (5, 6, 7):
+        for Nd in (5120, 17408):
+            packed, s = _rand_layer(wq, torch, Nd, K, bits, gen)
+            x = torch.randn(64, K, device="cuda", generator=gen).to(torch.bfloat16)
+            y = torch.empty(64, Nd, dtype=torch.bfloat16, device="cuda")
+            ws = torch.zeros(max(1, wq.wna16_workspace_bytes(64, Nd, K, bits)), dtype=torch.uint8, device="cuda")
+            ms = _graph_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, Nd, K, bits, y=y, ws=ws), 50)
+            rows.append(dict(bits=bits, N=Nd, M=64, **gbs(Nd * K * bits / 8, ms)))
+            del packed, s
+    out["decode_m64"] = rows
+
     # W4A8 (int8 activations quantized per token inside the call)
     packed, s = _rand_layer(wq, torch, N, K, 4, gen)
     rows = []
