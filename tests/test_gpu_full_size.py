@@ -2,7 +2,7 @@
 outputs that the oracle computes one by one (sampling output rows and tokens is
 exact: every output element depends only on its own weight row and token).
 
-Covered: the decode sweep (bits 5/6/7 x N 5120/17408 x M 1/4/16/64), the 8-bit
+Covered: the decode sweep (bits 5/6/7 x N 5120/17408 x M 1/4/16/32/64), the 8-bit
 lm_head (N = 248320, M = 1 and 4096), the quantized-embedding gather of 4096
 ids from the 248320-row table (bit-exact), W4A8 at M = 1 / 512 / 8192, and the
 64-layer mixed-bit stack (also replayed as one CUDA graph, which must give the
@@ -45,7 +45,7 @@ def test_decode_sweep_full_size(bits, N):
     s = I.make_scales(N, K // 128, 1100 + bits)
     packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(s), bits)
     ns = _sample(N, 64, bits + N, must=[0, N - 1])
-    for M in (1, 4, 16, 64):
+    for M in (1, 4, 16, 32, 64):
         x = I.make_x(M, K, 1200 + M)
         y = wq.wna16_gemm(to_dev_bf16(x), packed, s_dev, N, K, bits)
         torch.cuda.synchronize()

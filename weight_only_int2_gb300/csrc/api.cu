@@ -263,7 +263,7 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
   a.bits = bits;
   a.y = y;
   a.ws = static_cast<float*>(workspace);
-  cudaError_t e = use_prefill(M, N, K, bits) ? launch_prefill(c, x, Wpacked, scales, M, N, K, bits, y, nullptr)
+  cudaError_t e = use_prefill(M, N, K, bits, c.sm_count) ? launch_prefill(c, x, Wpacked, scales, M, N, K, bits, y, nullptr)
                                              : launch_stream_gemm(c, a);
   if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "wna16_gemm launch");
   return WQ_OK;
@@ -342,7 +342,7 @@ wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const
     if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "w4a8_gemm launch");
     return WQ_OK;
   }
-  if (use_prefill(M, N, K, 4)) {
+  if (use_prefill(M, N, K, 4, c.sm_count)) {
     // many tokens: codes as exact bf16 values into the tensor-core GEMM,
     // which applies sx per output row
     uint16_t* xqb = reinterpret_cast<uint16_t*>(sb);

@@ -91,8 +91,17 @@ bool prefill_supported(int64_t M, int64_t N, int64_t K, int bits);
 cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* packed, const uint16_t* scales,
                            int64_t M, int64_t N, int64_t K, int bits, uint16_t* y, const float* sx);
 
-inline bool use_prefill(int64_t M, int64_t N, int64_t K, int bits) {
-  return M >= kPrefillMinTokens && prefill_supported(M, N, K, bits);
+// From kPrefillMinTokens tokens on, always; from 32 tokens when the layer has
+// at least one 128-row tile per two SMs. Measured at K = 5120 (b = 5..7): the
+// tensor-core kernel takes ~41-43 us for any M in 17..64 (one CTA dequantizes
+// a whole row tile), the streaming kernel 41-46 us at M = 17..32 and 80 us at
+// M = 64 for 17408 rows, but 21-37 us for 5120 rows (40 tiles: 112 SMs idle
+// in the tensor-core kernel). The workspace queries keep sizing the
+// streaming kernel below kPrefillMinTokens, an upper bound either way.
+inline bool use_prefill(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
+  if (!prefill_supported(M, N, K, bits)) return false;
+  if (M >= kPrefillMinTokens) return true;
+  return M >= 32 && 2 * ((N + 127) / 128) >= sm_count;
 }
 
 // Decode by CTA pairs (M <= 16, K % 1024 == 0): no workspace, no grid-wide
