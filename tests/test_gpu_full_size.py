@@ -4,7 +4,7 @@ exact: every output element depends only on its own weight row and token).
 
 Covered: the decode sweep (bits 5/6/7 x N 5120/17408 x M 1/4/16/32/64), the 8-bit
 lm_head (N = 248320, M = 1 and 4096), the quantized-embedding gather of 4096
-ids from the 248320-row table (bit-exact), W4A8 at M = 1 / 512 / 8192, and the
+ids from the 248320-row table (bit-exact), W4A8 at M = 1 / 16 / 32 / 512 / 8192, and the
 64-layer mixed-bit stack (also replayed as one CUDA graph, which must give the
 same bits as eager execution)."""
 
@@ -88,7 +88,7 @@ def test_gather_full_size(vocab_table):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("M", [1, 512, 8192])
+@pytest.mark.parametrize("M", [1, 16, 32, 512, 8192])
 def test_w4a8_full_size(M):
     N = 17408
     q = I.make_codes(N, K, 4, 2300)
