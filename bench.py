@@ -358,10 +358,15 @@ def _rand_layer(wq, torch, N, K, bits, gen):
     return packed, s
 
 
-def _time_extras(wq, torch, stream):
+def _time_extras(wq, torch, stream, only=None):
     """The other rows of the scope table, each against its roofline: prefill
-    sweep, W4A8, the 8-bit lm_head, the embedding gather and the 64-layer
-    mixed-bit stack (timed as one CUDA graph)."""
+    sweep, the decode configuration's M = 64 cases, W4A8, the 8-bit lm_head,
+    the embedding gather and the 64-layer mixed-bit stack (timed as one CUDA
+    graph). `only` names one of them to time alone (profiling)."""
+
+    def want(name):
+        return only is None or only == name
+
     hbm, bf16, _, src = _peaks()
     gen = torch.Generator(device="cuda")
     gen.manual_seed(1234)
@@ -376,94 +381,117 @@ def _time_extras(wq, torch, stream):
         v = flops / (ms * 1e-3) / 1e12
         return {"ms": round(ms, 4), "TFLOPS": round(v, 1), "frac": round(v / bf16, 4)}
 
-    # prefill sweep: M in {2048, 8192} x bits in {5,6,7,8}, N = 17408
     N = 17408
-    rows = []
-    for bits in (5, 6, 7, 8):
-        packed, s = _rand_layer(wq, torch, N, K, bits, gen)
-        for M in (2048, 8192):
+    if want("prefill"):
+        # prefill sweep: M in {2048, 8192} x bits in {5,6,7,8}, N = 17408
+        rows = []
+        for bits in (5, 6, 7, 8):
+            packed, s = _rand_layer(wq, torch, N, K, bits, gen)
+            for M in (2048, 8192):
+                x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
+                y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+                ms = _event_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, N, K, bits, y=y), 3)
+                rows.append(dict(bits=bits, M=M, **tfl(2.0 * M * N * K, ms)))
+            del packed, s
+        out["prefill"] = rows
+
+    if want("decode_m64"):
+        # the decode configuration's M = 64 cases (outside the M <= 16 headline):
+        # the chunked streaming kernel, on packed-weight bytes
+        rows = []
+        for bits in (5, 6, 7):
+            for Nd in (5120, 17408):
+                packed, s = _rand_layer(wq, torch, Nd, K, bits, gen)
+                x = torch.randn(64, K, device="cuda", generator=gen).to(torch.bfloat16)
+                y = torch.empty(64, Nd, dtype=torch.bfloat16, device="cuda")
+                ws = torch.zeros(max(1, wq.wna16_workspace_bytes(64, Nd, K, bits)), dtype=torch.uint8, device="cuda")
+                ms = _graph_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, Nd, K, bits, y=y, ws=ws), 50)
+                rows.append(dict(bits=bits, N=Nd, M=64, **gbs(Nd * K * bits / 8, ms)))
+                del packed, s
+        out["decode_m64"] = rows
+
+    if want("w4a8"):
+        # W4A8 (int8 activations quantized per token inside the call)
+        packed, s = _rand_layer(wq, torch, N, K, 4, gen)
+        rows = []
+        for M in (1, 512, 8192):
             x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
             y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-            ms = _event_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, N, K, bits, y=y), 3)
-            rows.append(dict(bits=bits, M=M, **tfl(2.0 * M * N * K, ms)))
+            if M == 1:
+                ms = _graph_ms(torch, stream, lambda: wq.w4a8_gemm(x, packed, s, N, K, y=y), 200)
+                rows.append(dict(M=M, **gbs(N * K * 4 / 8, ms)))
+            else:
+                ms = _event_ms(torch, stream, lambda: wq.w4a8_gemm(x, packed, s, N, K, y=y), 3)
+                rows.append(dict(M=M, **tfl(2.0 * M * N * K, ms)))
+        out["w4a8"] = rows
         del packed, s
-    out["prefill"] = rows
 
-    # the decode configuration's M = 64 cases (outside the M <= 16 headline):
-    # the chunked streaming kernel, on packed-weight bytes
-    rows = []
-    for bits in (5, 6, 7):
-        for Nd in (5120, 17408):
-            packed, s = _rand_layer(wq, torch, Nd, K, bits, gen)
-            x = torch.randn(64, K, device="cuda", generator=gen).to(torch.bfloat16)
-            y = torch.empty(64, Nd, dtype=torch.bfloat16, device="cuda")
-            ws = torch.zeros(max(1, wq.wna16_workspace_bytes(64, Nd, K, bits)), dtype=torch.uint8, device="cuda")
-            ms = _graph_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, Nd, K, bits, y=y, ws=ws), 50)
-            rows.append(dict(bits=bits, N=Nd, M=64, **gbs(Nd * K * bits / 8, ms)))
-            del packed, s
-    out["decode_m64"] = rows
+    if want("lm_head") or want("gather"):
+        # lm_head: 8-bit, N = 248320 (1.27 GB packed), and the gather from the same table
+        V = 248320
+        packed, s = _rand_layer(wq, torch, V, K, 8, gen)
+        if want("lm_head"):
+            rows = []
+            for M in (1, 4096):
+                x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
+                y = torch.empty(M, V, dtype=torch.bfloat16, device="cuda")
+                if M == 1:
+                    ms = _graph_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, V, K, 8, y=y), 20)
+                    rows.append(dict(M=M, **gbs(V * K, ms)))
+                else:
+                    ms = _event_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, V, K, 8, y=y), 3)
+                    rows.append(dict(M=M, **tfl(2.0 * M * V * K, ms)))
+            out["lm_head"] = rows
+        if want("gather"):
+            T = 4096
+            ids = torch.randint(0, V, (T,), dtype=torch.int32, device="cuda", generator=gen)
+            ms = _graph_ms(torch, stream, lambda: wq.qembed_gather(ids, packed, s, V, K, 8), 100)
+            moved = T * (K + 2 * K // 128 + 2 * K + 4)  # packed row + scales in, bf16 row out, id
+            out["gather"] = dict(T=T, bytes_moved=moved, **gbs(moved, ms))
+        del packed, s
 
-    # W4A8 (int8 activations quantized per token inside the call)
-    packed, s = _rand_layer(wq, torch, N, K, 4, gen)
-    rows = []
-    for M in (1, 512, 8192):
-        x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
-        y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-        if M == 1:
-            ms = _graph_ms(torch, stream, lambda: wq.w4a8_gemm(x, packed, s, N, K, y=y), 200)
-            rows.append(dict(M=M, **gbs(N * K * 4 / 8, ms)))
-        else:
-            ms = _event_ms(torch, stream, lambda: wq.w4a8_gemm(x, packed, s, N, K, y=y), 3)
-            rows.append(dict(M=M, **tfl(2.0 * M * N * K, ms)))
-    out["w4a8"] = rows
-    del packed, s
+    if want("stack"):
+        # 64-layer stack: layers 0-9 and 54-63 at 7 bits, 10-53 alternating 5 / 6
+        layers = []
+        for li in range(64):
+            bits = 7 if (li < 10 or li >= 54) else (5 if (li - 10) % 2 == 0 else 6)
+            packed, s = _rand_layer(wq, torch, N, K, bits, gen)
+            layers.append((bits, packed, s))
+        stack_bytes = sum(N * K * b / 8 for b, _, _ in layers)
+        rows = []
+        for M in (1, 4096):
+            x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
+            ys = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
 
-    # lm_head: 8-bit, N = 248320 (1.27 GB packed), and the gather from the same table
-    V = 248320
-    packed, s = _rand_layer(wq, torch, V, K, 8, gen)
-    rows = []
-    for M in (1, 4096):
-        x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
-        y = torch.empty(M, V, dtype=torch.bfloat16, device="cuda")
-        if M == 1:
-            ms = _graph_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, V, K, 8, y=y), 20)
-            rows.append(dict(M=M, **gbs(V * K, ms)))
-        else:
-            ms = _event_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, V, K, 8, y=y), 3)
-            rows.append(dict(M=M, **tfl(2.0 * M * V * K, ms)))
-    out["lm_head"] = rows
-    T = 4096
-    ids = torch.randint(0, V, (T,), dtype=torch.int32, device="cuda", generator=gen)
-    ms = _graph_ms(torch, stream, lambda: wq.qembed_gather(ids, packed, s, V, K, 8), 100)
-    moved = T * (K + 2 * K // 128 + 2 * K + 4)  # packed row + scales in, bf16 row out, id
-    out["gather"] = dict(T=T, bytes_moved=moved, **gbs(moved, ms))
-    del packed, s
+            def stack():
+                for li, (b, pk, sc) in enumerate(layers):
+                    wq.wna16_gemm(x, pk, sc, N, K, b, y=ys[li & 1])
 
-    # 64-layer stack: layers 0-9 and 54-63 at 7 bits, 10-53 alternating 5 / 6
-    layers = []
-    for li in range(64):
-        bits = 7 if (li < 10 or li >= 54) else (5 if (li - 10) % 2 == 0 else 6)
-        packed, s = _rand_layer(wq, torch, N, K, bits, gen)
-        layers.append((bits, packed, s))
-    stack_bytes = sum(N * K * b / 8 for b, _, _ in layers)
-    rows = []
-    for M in (1, 4096):
-        x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
-        ys = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
-
-        def stack():
-            for li, (b, pk, sc) in enumerate(layers):
-                wq.wna16_gemm(x, pk, sc, N, K, b, y=ys[li & 1])
-
-        ms = _graph_ms(torch, stream, stack, 3 if M > 1 else 10)
-        if M == 1:
-            rows.append(dict(M=M, layers=64, packed_bytes=int(stack_bytes), **gbs(stack_bytes, ms)))
-        else:
-            rows.append(dict(M=M, layers=64, **tfl(2.0 * M * N * K * 64, ms)))
-    out["stack"] = rows
-    del layers
+            ms = _graph_ms(torch, stream, stack, 3 if M > 1 else 10)
+            if M == 1:
+                rows.append(dict(M=M, layers=64, packed_bytes=int(stack_bytes), **gbs(stack_bytes, ms)))
+            else:
+                rows.append(dict(M=M, layers=64, **tfl(2.0 * M * N * K * 64, ms)))
+        out["stack"] = rows
+        del layers
     torch.cuda.empty_cache()
     return out
+
+
+def run_only(args):
+    """One group of the other rows, timed alone (profiling): no decode sweep."""
+    import torch
+
+    import weight_only_int2_gb300 as wq
+    from weight_only_int2_gb300 import _build
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    _build.build()
+    wq.load()
+    stream = torch.cuda.Stream()
+    out = _time_extras(wq, torch, stream, only=args.only)
+    wq.check_status()
+    print(json.dumps({"only": args.only, **out}), flush=True)
 
 
 def run_prefill_case(args):
@@ -565,6 +593,8 @@ def main():
                     help="skip the other rows (prefill, W4A8, lm_head, gather, stack)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--only", choices=["prefill", "decode_m64", "w4a8", "lm_head", "gather", "stack"],
+                    default=None, help="time one group of the other rows alone, without the decode sweep")
     ap.add_argument("--prefill-case", type=str, default=None,
                     help="time one prefill shape 'bits,M' (N=17408, K=5120) alone (profiling)")
     ap.add_argument("--case", type=str, default=None,
@@ -578,6 +608,9 @@ def main():
                      f"M in {DECODE_M}")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.only is not None:
+        run_only(args)
+        return
     if args.prefill_case is not None:
         args.prefill_case = tuple(int(v) for v in args.prefill_case.split(","))
         if len(args.prefill_case) != 2 or not 2 <= args.prefill_case[0] <= 8 or args.prefill_case[1] < 1:

@@ -230,6 +230,24 @@ def test_gather_long_rows(bits):
     assert int(bad.item()) == nbad == 1
 
 
+@pytest.mark.parametrize("bits", [5, 8])
+def test_gather_tiny_and_huge_scales(bits):
+    """Scales whose products with (q - z) fall in the bf16 subnormal range
+    (2^-133 .. 2^-126), are subnormal themselves, or are very large: the
+    gather still rounds the exact product once, as the definition says."""
+    V, D = 6, 256
+    q = I.make_codes(V, D, bits, 95 + bits)
+    sv = np.array([2.0 ** -130, -(2.0 ** -133), 2.0 ** -125, 2.0 ** -120, 2.0 ** 100, -(2.0 ** 120)],
+                  dtype=np.float32)
+    s = np.repeat(O.f32_to_bf16_bits_rne(sv)[:, None], D // 128, axis=1).astype(np.uint16)
+    ids = np.arange(V, dtype=np.int32)
+    packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(s), bits)
+    out = wq.qembed_gather(to_dev(ids), packed, s_dev, V, D, bits)
+    torch.cuda.synchronize()
+    ref, _ = O.qembed_ref(ids, q, s, bits)
+    assert np.array_equal(bf16_dev_to_bits(out), ref)
+
+
 def test_gather_empty():
     packed, s_dev = wq.wna16_repack(to_dev(I.make_codes(4, 128, 8, 1)),
                                     to_dev_bf16(I.make_scales(4, 1, 2)), 8)

@@ -7,8 +7,11 @@
 // dense ceil(D*bits/32)-word rows directly, so every width works.
 //
 // out[t, d] = bf16_RNE(float(s[id, d/128]) * float(q[id, d] - 2^(bits-1))).
-// The float32 product is exact, so the single bf16 rounding matches the
-// definition; q == zero point with a negative scale yields -0.0.
+// The float32 product is exact, so one bf16 rounding of it is the definition.
+// It is computed as in the tensor-core GEMM's dequant: the codes in the
+// mantissa of bf16 128.0, an exact sub.bf16x2 of 128 + z, and a mul.bf16x2 by
+// the scale, which rounds the exact product once (no int-to-float
+// conversions); q == zero point with a negative scale yields -0.0.
 //
 // One CTA per token. Thread u reads the b words of its 32-code slice u
 // straight from global memory (the warp's loads cover one contiguous span of
@@ -17,6 +20,7 @@
 // barrier: any row length works, and no wait can stall.
 #include "wq_device.cuh"
 #include "wq_internal.h"
+#include "wq_dequant.cuh"
 
 namespace wq {
 namespace {
@@ -67,25 +71,15 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(
 
   const uint32_t* prow = packed + id * units * B;
   const uint16_t* srow = scales + id * (D / 128);
-  constexpr uint32_t kMask = (1u << B) - 1u;
-  constexpr int kZero = 1 << (B - 1);
   for (int64_t u = threadIdx.x; u < units; u += kThreads) {
     uint32_t win[B + 1];
     load_slice_words<B>(prow, u, win);
-    const float s = bf16_bits_to_float(__ldg(srow + (u >> 2)));
-    uint32_t o[16];
+    uint32_t w[B];
 #pragma unroll
-    for (int c = 0; c < 32; c += 2) {
-      const int p0 = c * B, p1 = (c + 1) * B;
-      const uint32_t a = ((p0 & 31) == 0) ? win[p0 >> 5]
-                                          : __funnelshift_r(win[p0 >> 5], win[(p0 >> 5) + 1], p0 & 31);
-      const uint32_t b = ((p1 & 31) == 0) ? win[p1 >> 5]
-                                          : __funnelshift_r(win[p1 >> 5], win[(p1 >> 5) + 1], p1 & 31);
-      const float f0 = s * static_cast<float>(static_cast<int>(a & kMask) - kZero);
-      const float f1 = s * static_cast<float>(static_cast<int>(b & kMask) - kZero);
-      const __nv_bfloat162 h = __floats2bfloat162_rn(f0, f1);
-      o[c >> 1] = *reinterpret_cast<const uint32_t*>(&h);
-    }
+    for (int i = 0; i < B; ++i) w[i] = win[i];
+    const uint32_t sb = __ldg(srow + (u >> 2));
+    uint32_t o[16];
+    dq::dequant_slice<B>(w, sb | (sb << 16), o);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
       orow[u * 4 + j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
