@@ -26,6 +26,7 @@ namespace wq {
 namespace {
 
 constexpr int kThreads = 128;
+constexpr size_t kStageMaxBytes = 48 * 1024;  // rows staged whole (no opt-in needed)
 
 // Words u * B .. u * B + B - 1 of a row (the row starts 16-byte aligned).
 template <int B>
@@ -50,17 +51,32 @@ __device__ __forceinline__ void load_slice_words(const uint32_t* __restrict__ ro
   w[B] = 0u;
 }
 
-template <int B>
+// Shared -> global bulk copy of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned), and the wait until it has read its shared-memory source.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// kStage: the output row is assembled in shared memory and written by one
+// bulk copy (rows up to kStageMaxBytes), instead of four 16-byte stores per
+// slice per thread, which fill the SM's global-memory instruction queue.
+template <int B, bool kStage>
 __global__ void __launch_bounds__(kThreads) gather_kernel(
     const int32_t* __restrict__ ids, const uint32_t* __restrict__ packed,
     const uint16_t* __restrict__ scales, int64_t V, int64_t D, uint16_t* __restrict__ out,
     int32_t* __restrict__ bad_count) {
+  extern __shared__ __align__(128) uint4 sout[];
   const int64_t t = blockIdx.x;
   const int64_t id = ids[t];
   const int64_t units = D / 32;
   uint4* orow = reinterpret_cast<uint4*>(out + t * D);
 
-  if (id < 0 || id >= V) {
+  if (id < 0 || id >= V) {  // the whole CTA
     for (int64_t u = threadIdx.x; u < units; u += kThreads) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) orow[u * 4 + j] = make_uint4(0u, 0u, 0u, 0u);
@@ -71,6 +87,7 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(
 
   const uint32_t* prow = packed + id * units * B;
   const uint16_t* srow = scales + id * (D / 128);
+  uint4* dst = kStage ? sout : orow;
   for (int64_t u = threadIdx.x; u < units; u += kThreads) {
     uint32_t win[B + 1];
     load_slice_words<B>(prow, u, win);
@@ -82,7 +99,15 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(
     dq::dequant_slice<B>(w, sb | (sb << 16), o);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      orow[u * 4 + j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+      dst[u * 4 + j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+  }
+  if constexpr (kStage) {
+    fence_proxy_async_smem();  // this thread's row bytes, before the copy reads them
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      bulk_store(orow, sout, static_cast<uint32_t>(D * 2));
+      bulk_store_wait_read();  // the shared memory stays valid until read
+    }
   }
 }
 
@@ -90,8 +115,13 @@ template <int B>
 cudaError_t launch_b(const Ctx& c, const int32_t* ids, int64_t T, const uint32_t* packed,
                      const uint16_t* scales, int64_t V, int64_t D, uint16_t* out,
                      int32_t* bad_count) {
-  gather_kernel<B><<<static_cast<unsigned>(T), kThreads, 0, c.stream>>>(ids, packed, scales, V, D, out,
-                                                                        bad_count);
+  const size_t row_bytes = static_cast<size_t>(D) * 2;
+  if (row_bytes <= kStageMaxBytes)
+    gather_kernel<B, true><<<static_cast<unsigned>(T), kThreads, row_bytes, c.stream>>>(ids, packed, scales, V, D,
+                                                                                       out, bad_count);
+  else
+    gather_kernel<B, false><<<static_cast<unsigned>(T), kThreads, 0, c.stream>>>(ids, packed, scales, V, D, out,
+                                                                                bad_count);
   return cudaGetLastError();
 }
 
