@@ -91,3 +91,27 @@ def test_bad_arguments_rejected_before_any_cuda_call(lib):
     assert b"workspace" in lib.wq_last_error()
     # gather: T = 0 is a no-op that needs no GPU
     assert lib.qembed_gather(None, 0, fake, fake, 10, 128, 8, 128, fake, None, None) == 0
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/wq.h is usable from C (not only C++): it compiles as C11 with
+    warnings as errors, and every entry point is callable through a pointer
+    of the declared type."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_wq.c"
+    src.write_text('#include "wq.h"\n'
+                   "int main(void) {\n"
+                   "  wq_status (*g)(const wq_bf16*, int64_t, const uint32_t*, const wq_bf16*, int64_t, int64_t,\n"
+                   "                 int, int, wq_bf16*, void*, size_t, void*) = wna16_gemm;\n"
+                   "  size_t (*w)(int64_t, int) = wq_packed_words_per_row;\n"
+                   "  return (g != 0 && w != 0) ? 0 : 1;\n"
+                   "}\n")
+    r = subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                        os.path.join(ROOT, "include"), "-c", str(src), "-o", str(tmp_path / "use_wq.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
