@@ -397,7 +397,7 @@ def _time_extras(wq, torch, stream, only=None):
 
     if want("decode_m64"):
         # the decode configuration's M = 64 cases (outside the M <= 16 headline):
-        # the chunked streaming kernel, on packed-weight bytes
+        # (streaming or tensor-core kernel by shape), on packed-weight bytes
         rows = []
         for bits in (5, 6, 7):
             for Nd in (5120, 17408):
