@@ -646,7 +646,7 @@ def main():
                 "data": "synthetic",
                 "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
                            "l2": "inputs larger than L2: each step reads 0.78 GB of distinct packed weights",
-                           "timing": "CUDA graph of one step, CUDA events between launches"},
+                           "timing": "CUDA events around K back-to-back replays of a CUDA graph of one step (18 launches); the per-case table replays a second graph with events between launches"},
                 "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"],
                 "gpu_launches": r["launches"], "clocks": r["clocks"], "extras": r["extras"],
                 "cases": r["cases"]}
