@@ -90,7 +90,10 @@ size_t wna16_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits);
  * float32 accumulation, y rounded to bf16 (round-to-nearest-even).
  *  x        [M, K] bf16.        Wpacked [N, ceil(K*bits/32)] uint32 (v1 layout).
  *  scales   [N, K/128] bf16.    y       [M, N] bf16 output.
- *  workspace, ws_bytes: device scratch of at least wna16_workspace_bytes();
+ *  workspace, ws_bytes: device scratch of at least wna16_workspace_bytes(),
+ *             an upper bound (a 32..64-token shape that runs on the
+ *             tensor-core kernel needs none: 32 <= M <= 64 on a layer with a
+ *             128-row tile for every two SMs);
  *             it must be zero-filled before its first use and every call that
  *             returns WQ_OK leaves it zero-filled again. Calls that may run
  *             concurrently must not share one workspace. May be NULL when the
@@ -110,7 +113,9 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
  * scratch is a fixed 4 MiB __device__ array owned by the library, held by
  * every GPU that loads it until the process exits.
  *  - Shapes whose wna16_workspace_bytes() exceeds 4 MiB (about M*N > 1M)
- *    return WQ_EINVAL with a message; use wna16_gemm for those.
+ *    return WQ_EINVAL with a message, unless they run on the tensor-core
+ *    kernel, which needs no scratch (32 <= M <= 64 on a layer with a
+ *    128-row tile for every two SMs); use wna16_gemm for the others.
  *  - The scratch region used is cleared on `stream` before the GEMM, so no
  *    state carries over between calls; calls whose executions overlap on the
  *    GPU (other streams, other host threads) share the array and race.

@@ -65,3 +65,34 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     st = lib.wna16_gemm_noalloc(fake, M, fake, fake, N, K, 8, 128, fake, None)
     assert st == 1
     assert b"scratch" in lib.wq_last_error()
+
+
+def test_tensor_core_shapes_need_no_scratch():
+    """64 tokens on a 17408-row layer run on the tensor-core kernel, which
+    needs no workspace: wna16_gemm accepts a NULL workspace and the
+    allocation-free entry point accepts the shape although the workspace
+    query (an upper bound) exceeds its 4 MiB array. Same kernel, same bits."""
+    lib = wq.load()
+    M, N, K, bits = 64, 17408, 5120, 6
+    assert torch.cuda.get_device_properties(0).multi_processor_count <= 2 * ((N + 127) // 128)
+    assert lib.wna16_workspace_bytes(M, N, K, bits) > (4 << 20)
+    x = I.make_x(M, K, 510)
+    q = I.make_codes(N, K, bits, 511)
+    s = I.make_scales(N, K // 128, 512)
+    packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(s), bits)
+    xd = to_dev_bf16(x)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    y_ws = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    st = lib.wna16_gemm(ctypes.c_void_p(xd.data_ptr()), M, ctypes.c_void_p(packed.data_ptr()),
+                        ctypes.c_void_p(s_dev.data_ptr()), N, K, bits, 128, ctypes.c_void_p(y_ws.data_ptr()),
+                        None, 0, stream)
+    assert st == 0, lib.wq_last_error().decode()
+    y_na = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    _call_noalloc(lib, xd, packed, s_dev, N, K, bits, y_na)
+    torch.cuda.synchronize()
+    assert torch.equal(y_ws.view(torch.int16), y_na.view(torch.int16))
+    ms = np.array([0, 17, 63])
+    ns = np.array([0, 5000, N - 1])
+    got = y_ws[torch.as_tensor(ms, device="cuda")][:, torch.as_tensor(ns, device="cuda")]
+    assert_bf16_close(got, O.wna16_ref(x[ms], q[ns], s[ns], bits), "tensor-core route, no workspace")
+    wq.check_status()

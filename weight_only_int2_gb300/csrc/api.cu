@@ -244,14 +244,22 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
   WQ_PTR(Wpacked);
   WQ_PTR(scales);
   WQ_PTR(y);
+  // The workspace the streaming kernel needs; a 32..64-token shape that the
+  // tensor-core kernel may take is checked once the SM count is known.
   const size_t need = stream_workspace_bytes(M, N, K);
-  if (need > 0) {
+  const bool maybe_tc = M >= 32 && M < kPrefillMinTokens && prefill_supported(M, N, K, bits);
+  if (need > 0 && !maybe_tc) {
     WQ_PTR(workspace);
     if (ws_bytes < need)
       return fail(WQ_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
   }
   Ctx c{};
   WQ_TRY(get_ctx(stream, &c));
+  if (need > 0 && maybe_tc && !use_prefill(M, N, K, bits, c.sm_count)) {
+    WQ_PTR(workspace);
+    if (ws_bytes < need)
+      return fail(WQ_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  }
   GemvArgs a{};
   a.mode = GemvMode::kWna16;
   a.x = x;

@@ -40,9 +40,13 @@ using namespace wq;
 extern "C" wq_status wna16_gemm_noalloc(const wq_bf16* x, int64_t M, const uint32_t* Wpacked,
                                         const wq_bf16* scales, int64_t N, int64_t K, int bits, int group,
                                         wq_bf16* y, void* stream) {
-  // The same argument checks as wna16_gemm, plus the scratch limit.
-  const size_t need = wna16_workspace_bytes(M, N, K, bits);
-  if (need > kNoAllocScratchBytes) {
+  // The same argument checks as wna16_gemm, plus the scratch limit. A
+  // 32..64-token shape that the tensor-core kernel takes needs no scratch;
+  // that is known once the device's SM count is.
+  size_t need = wna16_workspace_bytes(M, N, K, bits);
+  const bool maybe_tc = M >= 32 && M < kPrefillMinTokens && bits >= 2 && bits <= 8 && group == 128 &&
+                        prefill_supported(M, N, K, bits);
+  if (need > kNoAllocScratchBytes && !maybe_tc) {
     set_error("wna16_gemm_noalloc: this shape needs %zu bytes of scratch, above the fixed %zu-byte array "
               "(use wna16_gemm with a caller-provided workspace)",
               need, kNoAllocScratchBytes);
@@ -53,6 +57,21 @@ extern "C" wq_status wna16_gemm_noalloc(const wq_bf16* x, int64_t M, const uint3
   if (e != cudaSuccess) {
     set_error("wna16_gemm_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
     return WQ_ECUDA;
+  }
+  if (maybe_tc) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+      set_error("wna16_gemm_noalloc: SM count: %s", cudaGetErrorString(e));
+      return WQ_ECUDA;
+    }
+    if (use_prefill(M, N, K, bits, sms)) need = 0;
+    if (need > kNoAllocScratchBytes) {
+      set_error("wna16_gemm_noalloc: this shape needs %zu bytes of scratch, above the fixed %zu-byte array "
+                "(use wna16_gemm with a caller-provided workspace)",
+                need, kNoAllocScratchBytes);
+      return WQ_EINVAL;
+    }
   }
   if (dev < 0 || dev >= kMaxDev) {
     set_error("wna16_gemm_noalloc: device index %d too large", dev);
