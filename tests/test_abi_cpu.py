@@ -115,3 +115,42 @@ def test_header_is_plain_c(tmp_path):
                         os.path.join(ROOT, "include"), "-c", str(src), "-o", str(tmp_path / "use_wq.o")],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """There is no fallback path: without libwq.so the binding refuses to load."""
+    import subprocess
+    import sys
+
+    code = ("import weight_only_int2_gb300._lib as L\n"
+            "try:\n"
+            "    L.load(%r)\n"
+            "except RuntimeError as e:\n"
+            "    print('refused:', e)\n" % str(tmp_path / "libwq.so"))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert "refused: libwq.so not found" in r.stdout
+
+
+def test_host_tensors_are_refused(lib):
+    """The entry points take device tensors only; host tensors raise before
+    any work instead of being computed somewhere else."""
+    import torch
+
+    import weight_only_int2_gb300 as wq
+
+    bits, N, K = 6, 8, 128
+    x = torch.zeros(1, K, dtype=torch.bfloat16)
+    packed = torch.zeros(N, wq.packed_words_per_row(K, bits), dtype=torch.int32)
+    scales = torch.zeros(N, K // 128, dtype=torch.bfloat16)
+    codes = torch.zeros(N, K, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        wq.wna16_gemm(x, packed, scales, N, K, bits)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        wq.wna16_repack(codes, scales, bits)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        wq.act_quant_int8(x)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        wq.w4a8_gemm(x, torch.zeros(N, wq.packed_words_per_row(K, 4), dtype=torch.int32), scales, N, K)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        wq.qembed_gather(torch.zeros(2, dtype=torch.int32), packed, scales, N, K, bits)
