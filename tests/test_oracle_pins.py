@@ -221,6 +221,52 @@ def test_act_quant_invariants():
         assert np.all(err <= 0.5 * np.float64(sx[m]) * (1 + 1e-6))
 
 
+def _nearest_f32(q: Fraction) -> np.float32:
+    """The float32 nearest to the rational q, ties to the even significand:
+    IEEE round-to-nearest of an exact quotient, decided by comparing exact
+    distances of the float32 values around float(q)."""
+    f = np.float32(float(q))
+    cands = [np.nextafter(f, np.float32(-np.inf)), f, np.nextafter(f, np.float32(np.inf))]
+    return min(cands, key=lambda c: (abs(Fraction(float(c)) - q),
+                                     int(np.array([c], dtype=np.float32).view(np.uint32)[0]) & 1))
+
+
+def _round_half_even(v: Fraction) -> int:
+    lo = v.numerator // v.denominator
+    d = v - lo
+    if d != Fraction(1, 2):
+        return lo + (d > Fraction(1, 2))
+    return lo + (lo % 2)
+
+
+def test_act_quant_is_ieee_division_then_round_half_even():
+    """In exact rational arithmetic: sx is amax / 127 rounded once to
+    float32; xq is x / sx rounded once to float32, then to the nearest
+    integer, ties to even, clamped to +-127 ("int8 activations (W4A8)"
+    discussion, "Under the hood": per-token dynamic int8; the division and
+    rounding details are this oracle's stated reading). Row m holds amax and
+    +-amax/2 for every bf16 amax in [64, 128): x / sx then lies within
+    rounding of 63.5, where a reciprocal multiply or a second rounding step
+    decides differently for some rows."""
+    rows = []
+    extra = O.bf16_bits_to_f32(I.make_x(128, 4, 57))          # |x| < 64
+    for m in range(128):
+        a = float(O.bf16_bits_to_f32(np.array([0x4280 | m], dtype=np.uint16))[0])
+        row = [a, a / 2, -a / 2, a / 4] + extra[m].tolist()
+        rows.append([-v for v in row] if m % 2 else row)
+    x = _bf16(rows)
+    xq, sx = O.act_quant_ref(x)
+    xf = O.bf16_bits_to_f32(x)
+    for m in range(len(rows)):
+        amax = max(abs(Fraction(float(v))) for v in xf[m])
+        s = _nearest_f32(amax / 127)
+        assert sx[m] == s
+        for k in range(xf.shape[1]):
+            ratio = _nearest_f32(Fraction(float(xf[m, k])) / Fraction(float(s)))
+            want = max(-127, min(127, _round_half_even(Fraction(float(ratio)))))
+            assert int(xq[m, k]) == want, (m, k)
+
+
 def test_w4a8_group_acc_sums_to_integer_matmul_and_unit_scales():
     M, K, N = 4, 384, 5
     x = I.make_x_outliers(M, K, 61)
@@ -235,6 +281,29 @@ def test_w4a8_group_acc_sums_to_integer_matmul_and_unit_scales():
     assert np.array_equal(y, full.astype(np.float64))
     # widening is lossless: q - 8 covers [-8, 7] exactly
     assert (q.astype(np.int64) - 8).min() >= -8 and (q.astype(np.int64) - 8).max() <= 7
+
+
+def test_w4a8_brute_force_exact_rationals():
+    """Tiny W4A8 layer summed term by term in exact rationals: the integer
+    group sums over k // 128, each scaled by the token's float32 scale and the
+    group's bf16 scale ("int8 activations (W4A8)" discussion, "Under the hood":
+    integer accumulation of widened int4 weights, then the scales)."""
+    M, K, N = 2, 384, 3
+    x = I.make_x_outliers(M, K, 65)
+    q = I.make_codes(N, K, 4, 66)
+    s = I.make_scales(N, K // 128, 67)
+    xq, sx = O.act_quant_ref(x)
+    y = O.w4a8_ref_from_quant(xq, sx, q, s)
+    for m in range(M):
+        for n in range(N):
+            exact = Fraction(0)
+            mag = Fraction(0)
+            for g in range(K // 128):
+                acc = sum(int(xq[m, k]) * (int(q[n, k]) - 8) for k in range(128 * g, 128 * g + 128))
+                term = Fraction(float(sx[m])) * _frac_bf16(s[n, g]) * acc
+                exact += term
+                mag += abs(term)
+            assert abs(Fraction(float(y[m, n])) - exact) <= mag * Fraction(1, 2**45)
 
 
 def test_w4a8_close_to_wna16_b4():
