@@ -82,7 +82,11 @@ wq_status wna16_repack(const uint8_t* codes, const wq_bf16* scales, int64_t N, i
                        int bits, int group, uint32_t* packed, wq_bf16* scales_out,
                        int32_t* bad_count, void* stream);
 
-/* Bytes of workspace wna16_gemm needs for this shape (0 when none). */
+/* Bytes of workspace wna16_gemm needs for this shape, without asking the
+ * device: 0 when no GPU sends the shape to a split-K streaming kernel (65 or
+ * more tokens, or a few-token shape the CTA-pair decode kernel takes whatever
+ * the SM count); otherwise enough for either streaming kernel (an upper bound
+ * for 32..64 tokens; see wna16_gemm). wq_debug_route names the kernel. */
 size_t wna16_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits);
 
 /* WNA16 linear layer [INT57 s.1, CARD]:
@@ -97,7 +101,8 @@ size_t wna16_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits);
  *             it must be zero-filled before its first use and every call that
  *             returns WQ_OK leaves it zero-filled again. Calls that may run
  *             concurrently must not share one workspace. May be NULL when the
- *             required size is 0.
+ *             required size is 0, or when the kernel the call takes uses none;
+ *             a call whose kernel uses one returns WQ_EINVAL without it.
  *  M >= 1, N >= 1, bits in 2..8. */
 wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const wq_bf16* scales,
                      int64_t N, int64_t K, int bits, int group, wq_bf16* y,
@@ -150,8 +155,8 @@ size_t w4a8_scratch_bytes(int64_t M, int64_t K);
  *   acc[m, n, g] = sum_{k in group g} xq[m, k] * (q[n, k] - 8)   (exact, int32)
  *   y[m, n] = bf16( sx[m] * sum_g s[n, g] * acc[m, n, g] ).
  *  Wpacked4 [N, K/8] uint32 (v1 layout, bits = 4); scales [N, K/128] bf16.
- *  workspace, ws_bytes: at least w4a8_workspace_bytes(); zero-fill contract
- *             as for wna16_gemm (may be NULL when that size is 0).
+ *  workspace, ws_bytes: at least w4a8_workspace_bytes(); zero-fill and NULL
+ *             contract as for wna16_gemm.
  *  scratch, scratch_bytes: at least w4a8_scratch_bytes(); must not overlap the
  *             workspace. */
 wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const wq_bf16* scales,
@@ -181,6 +186,18 @@ wq_status qembed_gather(const int32_t* ids, int64_t T, const uint32_t* Wpacked,
  * after the first are meaningful only when it is 1. WQ_EINVAL for bits
  * outside 2..8, sm_count < 1 or a NULL out14. */
 wq_status wq_debug_decode_plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count, int64_t* out14);
+
+/* Which kernel wna16_gemm (w4a8 = 0) or w4a8_gemm (w4a8 = 1, bits = 4) launches
+ * for a shape on a device with sm_count SMs (host only, no device call). The
+ * entry points dispatch on the same function. *route receives one of: */
+#define WQ_ROUTE_DECODE_PAIR 1   /* CTA-pair decode kernel: M <= 16, K % 1024 == 0 */
+#define WQ_ROUTE_DECODE_SPLITK 2 /* persistent split-K decode kernel (uses the workspace) */
+#define WQ_ROUTE_CHUNKED 3       /* chunked split-K streaming kernel (uses the workspace) */
+#define WQ_ROUTE_TENSOR_CORE 4   /* tcgen05 tensor-core GEMM: M >= 65, or 32..64 tokens on a
+                                    layer with a 128-row tile for every two SMs */
+/* WQ_EINVAL for a NULL route, sm_count < 1, w4a8 not 0/1, bits outside 2..8
+ * (not 4 with w4a8), K not a positive multiple of 128, or M, N < 1. */
+wq_status wq_debug_route(int64_t M, int64_t N, int64_t K, int bits, int w4a8, int sm_count, int* route);
 
 /* Inverse of the repack for the codes: packed [N, ceil(K*bits/32)] ->
  * codes [N, K] uint8. */

@@ -89,6 +89,12 @@ def test_bad_arguments_rejected_before_any_cuda_call(lib):
     assert lib.wna16_workspace_bytes(1, 5120, 2560, 6) > 16  # else the call below would launch
     assert lib.wna16_gemm(fake, 1, fake, fake, 5120, 2560, 6, 128, fake, fake, 16, None) == 1
     assert b"workspace" in lib.wq_last_error()
+    # a decode-sized call whose K half does not fit the pair kernel's shared
+    # memory streams through the split-K kernel: the query says so, and a
+    # missing workspace is refused
+    assert lib.wna16_workspace_bytes(1, 8, 65536, 2) > 0
+    assert lib.wna16_gemm(fake, 1, fake, fake, 8, 65536, 2, 128, fake, None, 0, None) == 1
+    assert b"workspace is NULL" in lib.wq_last_error()
     # gather: T = 0 is a no-op that needs no GPU
     assert lib.qembed_gather(None, 0, fake, fake, 10, 128, 8, 128, fake, None, None) == 0
 

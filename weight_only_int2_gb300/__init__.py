@@ -9,7 +9,9 @@ from ._lib import (  # noqa: F401
     WQError,
     act_quant_int8,
     check_status,
+    ROUTES,
     debug_decode_plan,
+    debug_route,
     debug_unpack,
     debug_w4a8_group_acc,
     load,

@@ -41,6 +41,7 @@ SIGNATURES = {
     "qembed_gather": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_int, _c_int, _c_ptr,
                                _c_ptr, _c_ptr]),
     "wq_debug_decode_plan": (_c_int, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_ptr]),
+    "wq_debug_route": (_c_int, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_ptr]),
     "wq_debug_unpack": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr]),
     "wq_debug_w4a8_group_acc": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr]),
     "wq_check_status": (_c_int, []),
@@ -277,6 +278,17 @@ def debug_decode_plan(M: int, N: int, K: int, bits: int, sm_count: int) -> dict:
     out = (ctypes.c_int64 * len(_PLAN_KEYS))()
     _check(load().wq_debug_decode_plan(M, N, K, bits, sm_count, ctypes.addressof(out)), "wq_debug_decode_plan")
     return dict(zip(_PLAN_KEYS, (int(v) for v in out)))
+
+
+ROUTES = {1: "decode_pair", 2: "decode_splitk", 3: "chunked", 4: "tensor_core"}
+
+
+def debug_route(M: int, N: int, K: int, bits: int, sm_count: int, w4a8: bool = False) -> str:
+    """Which kernel wna16_gemm (or w4a8_gemm) launches for a shape on a device
+    with sm_count SMs (host only): one of the ROUTES names."""
+    out = ctypes.c_int(0)
+    _check(load().wq_debug_route(M, N, K, bits, int(bool(w4a8)), sm_count, ctypes.byref(out)), "wq_debug_route")
+    return ROUTES[out.value]
 
 
 def debug_unpack(packed: torch.Tensor, N: int, K: int, bits: int) -> torch.Tensor:

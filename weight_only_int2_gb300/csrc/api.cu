@@ -91,6 +91,20 @@ wq_status check_group_k(int group, int64_t K, const char* kname) {
   return WQ_OK;
 }
 
+// A split-K workspace: non-NULL, 16-byte aligned, at least `need` bytes.
+wq_status check_workspace(const void* workspace, size_t ws_bytes, size_t need) {
+  if (workspace == nullptr) return fail(WQ_EINVAL, "workspace is NULL");
+  if (!aligned16(workspace)) return fail(WQ_EINVAL, "workspace is not 16-byte aligned");
+  if (ws_bytes < need) return fail(WQ_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  return WQ_OK;
+}
+
+// A 32..64-token shape that the tensor-core kernel may take (decided with the
+// SM count): its workspace is checked only if the route turns out to use it.
+bool maybe_tensor_core(int64_t M, int64_t N, int64_t K, int bits) {
+  return M >= 32 && M < kPrefillMinTokens && prefill_supported(M, N, K, bits);
+}
+
 #define WQ_TRY(expr)            \
   do {                          \
     wq_status _s = (expr);      \
@@ -228,9 +242,8 @@ wq_status wna16_repack(const uint8_t* codes, const wq_bf16* scales, int64_t N, i
 }
 
 size_t wna16_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits) {
-  (void)bits;
   if (M < 1 || N < 1 || K < 128) return 0;
-  return stream_workspace_bytes(M, N, K);
+  return stream_workspace_bytes(M, N, K, bits);
 }
 
 wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const wq_bf16* scales,
@@ -244,22 +257,16 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
   WQ_PTR(Wpacked);
   WQ_PTR(scales);
   WQ_PTR(y);
-  // The workspace the streaming kernel needs; a 32..64-token shape that the
-  // tensor-core kernel may take is checked once the SM count is known.
-  const size_t need = stream_workspace_bytes(M, N, K);
-  const bool maybe_tc = M >= 32 && M < kPrefillMinTokens && prefill_supported(M, N, K, bits);
-  if (need > 0 && !maybe_tc) {
-    WQ_PTR(workspace);
-    if (ws_bytes < need)
-      return fail(WQ_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
-  }
+  // The documented size is checked before any device call, except for a
+  // 32..64-token shape the tensor-core GEMM may take (known from the SM
+  // count); then the route's own need, whatever the query said.
+  const size_t need = stream_workspace_bytes(M, N, K, bits);
+  if (need > 0 && !maybe_tensor_core(M, N, K, bits)) WQ_TRY(check_workspace(workspace, ws_bytes, need));
   Ctx c{};
   WQ_TRY(get_ctx(stream, &c));
-  if (need > 0 && maybe_tc && !use_prefill(M, N, K, bits, c.sm_count)) {
-    WQ_PTR(workspace);
-    if (ws_bytes < need)
-      return fail(WQ_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
-  }
+  const Route r = route_wna16(M, N, K, bits, c.sm_count);
+  const size_t need_r = route_workspace_bytes(r, M, N, K);
+  if (need_r > 0) WQ_TRY(check_workspace(workspace, ws_bytes, need_r));
   GemvArgs a{};
   a.mode = GemvMode::kWna16;
   a.x = x;
@@ -271,8 +278,8 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
   a.bits = bits;
   a.y = y;
   a.ws = static_cast<float*>(workspace);
-  cudaError_t e = use_prefill(M, N, K, bits, c.sm_count) ? launch_prefill(c, x, Wpacked, scales, M, N, K, bits, y, nullptr)
-                                             : launch_stream_gemm(c, a);
+  cudaError_t e = r == Route::kTensorCore ? launch_prefill(c, x, Wpacked, scales, M, N, K, bits, y, nullptr)
+                                          : launch_routed(c, r, a);
   if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "wna16_gemm launch");
   return WQ_OK;
 }
@@ -296,7 +303,7 @@ static size_t al256(size_t v) { return (v + 255) / 256 * 256; }
 
 size_t w4a8_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (M < 1 || N < 1 || K < 128) return 0;
-  return stream_workspace_bytes(M, N, K);
+  return stream_workspace_bytes(M, N, K, 4);
 }
 
 size_t w4a8_scratch_bytes(int64_t M, int64_t K) {
@@ -316,41 +323,41 @@ wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const
   WQ_PTR(scales);
   WQ_PTR(y);
   WQ_PTR(scratch);
-  const size_t need = w4a8_workspace_bytes(M, N, K);
-  if (need > 0) {
-    WQ_PTR(workspace);
-    if (ws_bytes < need) return fail(WQ_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
-  }
   const size_t need_s = w4a8_scratch_bytes(M, K);
   if (scratch_bytes < need_s)
     return fail(WQ_EINVAL, "scratch too small: %zu < %zu bytes", scratch_bytes, need_s);
-  if (need > 0) {
-    const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), s0 = reinterpret_cast<uintptr_t>(scratch);
-    if (w0 < s0 + need_s && s0 < w0 + need) return fail(WQ_EINVAL, "scratch overlaps the workspace");
-  }
+  const size_t need = w4a8_workspace_bytes(M, N, K);
+  if (need > 0 && !maybe_tensor_core(M, N, K, 4)) WQ_TRY(check_workspace(workspace, ws_bytes, need));
   Ctx c{};
   WQ_TRY(get_ctx(stream, &c));
+  const Route r = route_w4a8(M, N, K, c.sm_count);
+  const size_t need_r = route_workspace_bytes(r, M, N, K);
+  if (need_r > 0) {
+    WQ_TRY(check_workspace(workspace, ws_bytes, need_r));
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), s0 = reinterpret_cast<uintptr_t>(scratch);
+    if (w0 < s0 + need_s && s0 < w0 + need_r) return fail(WQ_EINVAL, "scratch overlaps the workspace");
+  }
   uint8_t* sb = static_cast<uint8_t*>(scratch);
   int8_t* xq = reinterpret_cast<int8_t*>(sb);
   float* sx = reinterpret_cast<float*>(sb + al256(static_cast<size_t>(M) * K * 2));
-  if (decode2_supported(M, N, K, 4, c.sm_count)) {
+  GemvArgs a{};
+  a.mode = GemvMode::kW4a8;
+  a.packed = Wpacked4;
+  a.scales = scales;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bits = 4;
+  a.y = y;
+  if (r == Route::kDecodePair) {
     // few tokens: the decode kernel quantizes the activations per token in
     // its staging (same arithmetic as act_quant_int8), no separate pass
-    GemvArgs a{};
-    a.mode = GemvMode::kW4a8;
     a.x = x;
-    a.packed = Wpacked4;
-    a.scales = scales;
-    a.M = M;
-    a.N = N;
-    a.K = K;
-    a.bits = 4;
-    a.y = y;
     cudaError_t e = launch_decode2(c, a);
     if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "w4a8_gemm launch");
     return WQ_OK;
   }
-  if (use_prefill(M, N, K, 4, c.sm_count)) {
+  if (r == Route::kTensorCore) {
     // many tokens: codes as exact bf16 values into the tensor-core GEMM,
     // which applies sx per output row
     uint16_t* xqb = reinterpret_cast<uint16_t*>(sb);
@@ -362,19 +369,10 @@ wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const
   }
   cudaError_t e = launch_act_quant(c, x, M, K, xq, sx);
   if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
-  GemvArgs a{};
-  a.mode = GemvMode::kW4a8;
   a.xq = xq;
   a.sx = sx;
-  a.packed = Wpacked4;
-  a.scales = scales;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.bits = 4;
-  a.y = y;
   a.ws = static_cast<float*>(workspace);
-  e = launch_stream_gemm(c, a);
+  e = launch_routed(c, r, a);
   if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "w4a8_gemm launch");
   return WQ_OK;
 }
@@ -403,6 +401,23 @@ wq_status wq_debug_decode_plan(int64_t M, int64_t N, int64_t K, int bits, int sm
   WQ_PTR(out14);
   if (bits < 2 || bits > 8 || sm_count < 1) return fail(WQ_EINVAL, "bits must be in 2..8 and sm_count >= 1");
   decode2_plan_info(M, N, K, bits, sm_count, out14);
+  return WQ_OK;
+}
+
+wq_status wq_debug_route(int64_t M, int64_t N, int64_t K, int bits, int w4a8, int sm_count, int* route) {
+  t_err[0] = 0;
+  if (route == nullptr) return fail(WQ_EINVAL, "route is NULL");
+  if (sm_count < 1) return fail(WQ_EINVAL, "sm_count must be >= 1");
+  if (w4a8 != 0 && w4a8 != 1) return fail(WQ_EINVAL, "w4a8 must be 0 or 1");
+  if (w4a8) {
+    if (bits != 4) return fail(WQ_EINVAL, "W4A8 weights are 4-bit (got bits = %d)", bits);
+  } else {
+    WQ_TRY(check_bits(bits));
+  }
+  WQ_TRY(check_group_k(128, K, "K"));
+  if (M < 1 || N < 1) return fail(WQ_EINVAL, "M and N must be >= 1");
+  const Route r = w4a8 ? route_w4a8(M, N, K, sm_count) : route_wna16(M, N, K, bits, sm_count);
+  *route = static_cast<int>(r);
   return WQ_OK;
 }
 

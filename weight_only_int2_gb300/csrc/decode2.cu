@@ -730,6 +730,20 @@ bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count) 
 
 bool decode2_shape(int64_t M, int64_t K) { return M >= 1 && M <= 16 && K >= 1024 && K % 1024 == 0; }
 
+// The plan exists on every device with at least two SMs when its smallest
+// configuration (ksplit 1, two ring slots) fits at the largest chunk any SM
+// count gives: a chunk has at most min(N, kMaxH) rows, and the shared-memory
+// footprint grows with the rows, the tiles and the ring depth.
+bool decode2_fits_any(int64_t M, int64_t N, int64_t K, int bits) {
+  if (bits < 2 || bits > 8 || !decode2_shape(M, K) || N < 1 || N >= (int64_t(1) << 31)) return false;
+  const int G = static_cast<int>(K / 128), Gh = G / 2;
+  const int sx0 = (Gh / 8) * 8, sbox = ((G - sx0 + 7) / 8) * 8;
+  if (sbox < Gh || sbox > 256) return false;
+  const int H = static_cast<int>(N < kMaxH ? N : kMaxH);
+  const int T = (H + kTileRows - 1) / kTileRows;
+  return d2_smem(bits, M <= 8 ? 1 : 2, T, H, Gh, sbox, 2).total <= kSmemCap;
+}
+
 int decode2_plan_info(int64_t M, int64_t N, int64_t K, int bits, int sm_count, int64_t* out) {
   const D2Plan pl = make_d2plan(M, N, K, bits, sm_count);
   const D2Params& p = pl.prm;

@@ -65,7 +65,7 @@ extern "C" wq_status wna16_gemm_noalloc(const wq_bf16* x, int64_t M, const uint3
       set_error("wna16_gemm_noalloc: SM count: %s", cudaGetErrorString(e));
       return WQ_ECUDA;
     }
-    if (use_prefill(M, N, K, bits, sms)) need = 0;
+    if (route_wna16(M, N, K, bits, sms) == Route::kTensorCore) need = 0;
     if (need > kNoAllocScratchBytes) {
       set_error("wna16_gemm_noalloc: this shape needs %zu bytes of scratch, above the fixed %zu-byte array "
                 "(use wna16_gemm with a caller-provided workspace)",

@@ -108,6 +108,8 @@ inline bool use_prefill(int64_t M, int64_t N, int64_t K, int bits, int sm_count)
 // synchronisation. Mode kWna16 (bf16 x), or kW4a8 with a.x the bf16
 // activations, which the kernel quantizes per token itself.
 bool decode2_shape(int64_t M, int64_t K);
+// Whether the pair kernel takes this shape whatever the device's SM count (>= 2).
+bool decode2_fits_any(int64_t M, int64_t N, int64_t K, int bits);
 // The CTA-pair decode plan for a shape, for host-side checks: out[14] =
 // {ok, C, H, nchunk, T, ksplit, NS, G, Gh, sbox, sx0, NT, smem bytes, max ring slots}.
 int decode2_plan_info(int64_t M, int64_t N, int64_t K, int bits, int sm_count, int64_t* out);
@@ -123,10 +125,57 @@ inline cudaError_t launch_stream_gemm(const Ctx& c, const GemvArgs& a) {
   return decode_supported(a.M, a.N, a.K, a.bits, c.sm_count) ? launch_decode(c, a) : launch_gemv(c, a);
 }
 
-// Workspace of the path a shape takes: none for the tensor-core GEMM and the
-// CTA-pair decode kernel.
-inline size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  if (M >= kPrefillMinTokens || decode2_shape(M, K)) return 0;
+// The kernel a GEMM call launches, by shape (host only). The entry points
+// dispatch on it and wq_debug_route reports it; the values are the header's
+// WQ_ROUTE_* numbers.
+enum class Route : int { kDecodePair = 1, kDecodeSplitK = 2, kChunked = 3, kTensorCore = 4 };
+
+inline Route route_stream(int64_t M, int64_t N, int64_t K, int bits, int sm_count, bool pair_ok) {
+  if (pair_ok && decode2_supported(M, N, K, bits, sm_count)) return Route::kDecodePair;
+  return decode_supported(M, N, K, bits, sm_count) ? Route::kDecodeSplitK : Route::kChunked;
+}
+
+inline Route route_wna16(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
+  if (use_prefill(M, N, K, bits, sm_count)) return Route::kTensorCore;
+  return route_stream(M, N, K, bits, sm_count, true);
+}
+
+// W4A8: the pair kernel quantizes few tokens itself; for many tokens the codes
+// go as exact bf16 values into the tensor-core kernel; otherwise int8 codes
+// feed the split-K streaming kernels.
+inline Route route_w4a8(int64_t M, int64_t N, int64_t K, int sm_count) {
+  if (decode2_supported(M, N, K, 4, sm_count)) return Route::kDecodePair;
+  if (use_prefill(M, N, K, 4, sm_count)) return Route::kTensorCore;
+  return route_stream(M, N, K, 4, sm_count, false);
+}
+
+// Launches a streaming route (every route but the tensor-core one, whose
+// kernel takes other arguments).
+inline cudaError_t launch_routed(const Ctx& c, Route r, const GemvArgs& a) {
+  switch (r) {
+    case Route::kDecodePair: return launch_decode2(c, a);
+    case Route::kDecodeSplitK: return launch_decode(c, a);
+    case Route::kChunked: return launch_gemv(c, a);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Workspace a route uses: the split-K partials and counters of the streaming
+// kernels; none for the pair kernel and the tensor-core GEMM.
+inline size_t route_workspace_bytes(Route r, int64_t M, int64_t N, int64_t K) {
+  if (r == Route::kChunked) return gemv_workspace_bytes(M, N, K);
+  if (r == Route::kDecodeSplitK) return decode_workspace_bytes(M, N);
+  return 0;
+}
+
+// The workspace query, without the SM count: zero when no SM count sends the
+// shape to a streaming kernel (65 or more tokens, or a shape the pair kernel
+// takes on every device); otherwise enough for either streaming kernel, an
+// upper bound for 32..64 tokens, which the tensor-core GEMM takes on layers
+// with a 128-row tile for every two SMs.
+inline size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits) {
+  if (M >= kPrefillMinTokens && prefill_supported(M, N, K, bits)) return 0;
+  if (decode2_fits_any(M, N, K, bits)) return 0;
   const size_t a = gemv_workspace_bytes(M, N, K), b = decode_workspace_bytes(M, N);
   return a > b ? a : b;
 }
