@@ -103,7 +103,10 @@ size_t wna16_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits);
  *             concurrently must not share one workspace. May be NULL when the
  *             required size is 0, or when the kernel the call takes uses none;
  *             a call whose kernel uses one returns WQ_EINVAL without it.
- *  M >= 1, N >= 1, bits in 2..8. */
+ *  M >= 1, N >= 1, bits in 2..8. Shapes that the tensor-core kernel does not
+ *  take (fewer than 65 tokens, see wq_debug_route) need K <= 16384 or, up to
+ *  16 tokens, K a multiple of 1024 whose activations fit the decode kernels;
+ *  others return WQ_EUNSUPPORTED. */
 wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const wq_bf16* scales,
                      int64_t N, int64_t K, int bits, int group, wq_bf16* y,
                      void* workspace, size_t ws_bytes, void* stream);
@@ -158,7 +161,8 @@ size_t w4a8_scratch_bytes(int64_t M, int64_t K);
  *  workspace, ws_bytes: at least w4a8_workspace_bytes(); zero-fill and NULL
  *             contract as for wna16_gemm.
  *  scratch, scratch_bytes: at least w4a8_scratch_bytes(); must not overlap the
- *             workspace. */
+ *             workspace.
+ *  The shape limits of wna16_gemm apply (WQ_EUNSUPPORTED). */
 wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const wq_bf16* scales,
                     int64_t N, int64_t K, int group, wq_bf16* y, void* workspace,
                     size_t ws_bytes, void* scratch, size_t scratch_bytes, void* stream);
@@ -190,6 +194,7 @@ wq_status wq_debug_decode_plan(int64_t M, int64_t N, int64_t K, int bits, int sm
 /* Which kernel wna16_gemm (w4a8 = 0) or w4a8_gemm (w4a8 = 1, bits = 4) launches
  * for a shape on a device with sm_count SMs (host only, no device call). The
  * entry points dispatch on the same function. *route receives one of: */
+#define WQ_ROUTE_NONE 0          /* no kernel takes the shape: the call returns WQ_EUNSUPPORTED */
 #define WQ_ROUTE_DECODE_PAIR 1   /* CTA-pair decode kernel: M <= 16, K % 1024 == 0 */
 #define WQ_ROUTE_DECODE_SPLITK 2 /* persistent split-K decode kernel (uses the workspace) */
 #define WQ_ROUTE_CHUNKED 3       /* chunked split-K streaming kernel (uses the workspace) */

@@ -280,7 +280,7 @@ def debug_decode_plan(M: int, N: int, K: int, bits: int, sm_count: int) -> dict:
     return dict(zip(_PLAN_KEYS, (int(v) for v in out)))
 
 
-ROUTES = {1: "decode_pair", 2: "decode_splitk", 3: "chunked", 4: "tensor_core"}
+ROUTES = {0: "none", 1: "decode_pair", 2: "decode_splitk", 3: "chunked", 4: "tensor_core"}
 
 
 def debug_route(M: int, N: int, K: int, bits: int, sm_count: int, w4a8: bool = False) -> str:

@@ -99,6 +99,14 @@ wq_status check_workspace(const void* workspace, size_t ws_bytes, size_t need) {
   return WQ_OK;
 }
 
+// The message of a shape no kernel takes.
+wq_status no_route(int64_t M, int64_t N, int64_t K) {
+  return fail(WQ_EUNSUPPORTED,
+              "no kernel takes M = %lld, N = %lld, K = %lld: below the tensor-core kernel's token counts "
+              "the streaming kernels take K <= 16384, or K a multiple of 1024 for up to 16 tokens",
+              (long long)M, (long long)N, (long long)K);
+}
+
 // A 32..64-token shape that the tensor-core kernel may take (decided with the
 // SM count): its workspace is checked only if the route turns out to use it.
 bool maybe_tensor_core(int64_t M, int64_t N, int64_t K, int bits) {
@@ -265,6 +273,7 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
   Ctx c{};
   WQ_TRY(get_ctx(stream, &c));
   const Route r = route_wna16(M, N, K, bits, c.sm_count);
+  if (r == Route::kNone) return no_route(M, N, K);
   const size_t need_r = route_workspace_bytes(r, M, N, K);
   if (need_r > 0) WQ_TRY(check_workspace(workspace, ws_bytes, need_r));
   GemvArgs a{};
@@ -331,6 +340,7 @@ wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const
   Ctx c{};
   WQ_TRY(get_ctx(stream, &c));
   const Route r = route_w4a8(M, N, K, c.sm_count);
+  if (r == Route::kNone) return no_route(M, N, K);
   const size_t need_r = route_workspace_bytes(r, M, N, K);
   if (need_r > 0) {
     WQ_TRY(check_workspace(workspace, ws_bytes, need_r));

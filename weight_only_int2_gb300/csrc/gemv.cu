@@ -380,6 +380,8 @@ cudaError_t launch_nt(const Ctx& c, const CUtensorMap& tmap, const Params& prm, 
 
 }  // namespace
 
+bool gemv_supported(int64_t K) { return K / 128 <= kMaxGroupsPerCta; }
+
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   (void)K;
   if (M > 64) return 0;

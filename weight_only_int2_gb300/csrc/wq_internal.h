@@ -76,6 +76,9 @@ struct GemvArgs {
 
 // Workspace bytes the weight-streaming GEMM needs for this shape.
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// Whether the chunked kernel takes K: a CTA keeps the scales of all its
+// groups in shared memory, at most 128 groups (K <= 16384).
+bool gemv_supported(int64_t K);
 
 cudaError_t launch_gemv(const Ctx& c, const GemvArgs& a);
 
@@ -128,11 +131,13 @@ inline cudaError_t launch_stream_gemm(const Ctx& c, const GemvArgs& a) {
 // The kernel a GEMM call launches, by shape (host only). The entry points
 // dispatch on it and wq_debug_route reports it; the values are the header's
 // WQ_ROUTE_* numbers.
-enum class Route : int { kDecodePair = 1, kDecodeSplitK = 2, kChunked = 3, kTensorCore = 4 };
+// kNone: no kernel takes the shape (the entry points return WQ_EUNSUPPORTED).
+enum class Route : int { kNone = 0, kDecodePair = 1, kDecodeSplitK = 2, kChunked = 3, kTensorCore = 4 };
 
 inline Route route_stream(int64_t M, int64_t N, int64_t K, int bits, int sm_count, bool pair_ok) {
   if (pair_ok && decode2_supported(M, N, K, bits, sm_count)) return Route::kDecodePair;
-  return decode_supported(M, N, K, bits, sm_count) ? Route::kDecodeSplitK : Route::kChunked;
+  if (decode_supported(M, N, K, bits, sm_count)) return Route::kDecodeSplitK;
+  return gemv_supported(K) ? Route::kChunked : Route::kNone;
 }
 
 inline Route route_wna16(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
