@@ -28,6 +28,8 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream);
  *    all work is enqueued asynchronously on it.
  *  - group must be 128 and K (or D) a positive multiple of 128.
+ *  - Sizes (M, N, K, T, V, D) are below 2^31; they become grid dimensions and
+ *    32-bit TMA coordinates. Larger values return WQ_EINVAL.
  *  - Return codes: WQ_OK, or WQ_EINVAL for bad arguments (returned
  *    synchronously, nothing enqueued), WQ_EUNSUPPORTED for a valid but
  *    unimplemented configuration, WQ_ECUDA when a CUDA call or a launch fails.

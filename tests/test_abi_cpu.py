@@ -95,6 +95,16 @@ def test_bad_arguments_rejected_before_any_cuda_call(lib):
     assert lib.wna16_workspace_bytes(1, 8, 65536, 2) > 0
     assert lib.wna16_gemm(fake, 1, fake, fake, 8, 65536, 2, 128, fake, None, 0, None) == 1
     assert b"workspace is NULL" in lib.wq_last_error()
+    # sizes at or above 2^31 (grid dimensions, 32-bit TMA coordinates)
+    big = 1 << 31
+    assert lib.wna16_gemm(fake, big, fake, fake, 8, 128, 6, 128, fake, None, 0, None) == 1
+    assert lib.wna16_gemm(fake, 1, fake, fake, big, 128, 6, 128, fake, None, 0, None) == 1
+    assert lib.wna16_gemm(fake, 1, fake, fake, 8, big, 6, 128, fake, None, 0, None) == 1
+    assert lib.act_quant_int8(fake, big, 128, fake, fake, None) == 1
+    assert lib.qembed_gather(fake, big, fake, fake, 10, 128, 8, 128, fake, None, None) == 1
+    assert lib.qembed_gather(fake, 4, fake, fake, big, 128, 8, 128, fake, None, None) == 1
+    assert lib.wna16_repack(fake, fake, big, 128, 6, 128, fake, fake, None, None) == 1
+    assert b"2^31" in lib.wq_last_error()
     # gather: T = 0 is a no-op that needs no GPU
     assert lib.qembed_gather(None, 0, fake, fake, 10, 128, 8, 128, fake, None, None) == 0
 

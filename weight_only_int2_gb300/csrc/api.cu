@@ -84,10 +84,18 @@ wq_status check_bits(int bits) {
   return WQ_OK;
 }
 
+// Sizes become grid dimensions and 32-bit TMA coordinates: all below 2^31.
+constexpr int64_t kMaxDim = 0x7FFFFFFF;
+
 wq_status check_group_k(int group, int64_t K, const char* kname) {
   if (group != 128) return fail(WQ_EUNSUPPORTED, "group must be 128 (got %d)", group);
-  if (K <= 0 || K % 128 != 0)
-    return fail(WQ_EINVAL, "%s must be a positive multiple of 128 (got %lld)", kname, (long long)K);
+  if (K <= 0 || K % 128 != 0 || K > kMaxDim)
+    return fail(WQ_EINVAL, "%s must be a positive multiple of 128 below 2^31 (got %lld)", kname, (long long)K);
+  return WQ_OK;
+}
+
+wq_status check_size(int64_t v, const char* name) {
+  if (v < 1 || v > kMaxDim) return fail(WQ_EINVAL, "%s must be in 1..2^31-1 (got %lld)", name, (long long)v);
   return WQ_OK;
 }
 
@@ -232,7 +240,7 @@ wq_status wna16_repack(const uint8_t* codes, const wq_bf16* scales, int64_t N, i
   t_err[0] = 0;
   WQ_TRY(check_bits(bits));
   WQ_TRY(check_group_k(group, K, "K"));
-  if (N < 1) return fail(WQ_EINVAL, "N must be >= 1");
+  WQ_TRY(check_size(N, "N"));
   WQ_PTR(codes);
   WQ_PTR(scales);
   WQ_PTR(packed);
@@ -260,7 +268,8 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
   t_err[0] = 0;
   WQ_TRY(check_bits(bits));
   WQ_TRY(check_group_k(group, K, "K"));
-  if (M < 1 || N < 1) return fail(WQ_EINVAL, "M and N must be >= 1");
+  WQ_TRY(check_size(M, "M"));
+  WQ_TRY(check_size(N, "N"));
   WQ_PTR(x);
   WQ_PTR(Wpacked);
   WQ_PTR(scales);
@@ -296,8 +305,8 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
 wq_status act_quant_int8(const wq_bf16* x, int64_t M, int64_t K, int8_t* xq, float* sx,
                          void* stream) {
   t_err[0] = 0;
-  if (M < 1) return fail(WQ_EINVAL, "M must be >= 1");
-  if (K <= 0 || K % 128 != 0) return fail(WQ_EINVAL, "K must be a positive multiple of 128");
+  WQ_TRY(check_size(M, "M"));
+  WQ_TRY(check_group_k(128, K, "K"));
   WQ_PTR(x);
   WQ_PTR(xq);
   WQ_PTR(sx);
@@ -326,7 +335,8 @@ wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const
                     void* scratch, size_t scratch_bytes, void* stream) {
   t_err[0] = 0;
   WQ_TRY(check_group_k(group, K, "K"));
-  if (M < 1 || N < 1) return fail(WQ_EINVAL, "M and N must be >= 1");
+  WQ_TRY(check_size(M, "M"));
+  WQ_TRY(check_size(N, "N"));
   WQ_PTR(x);
   WQ_PTR(Wpacked4);
   WQ_PTR(scales);
@@ -393,7 +403,8 @@ wq_status qembed_gather(const int32_t* ids, int64_t T, const uint32_t* Wpacked, 
   t_err[0] = 0;
   WQ_TRY(check_bits(bits));
   WQ_TRY(check_group_k(group, D, "D"));
-  if (T < 0 || V < 1) return fail(WQ_EINVAL, "T must be >= 0 and V >= 1");
+  if (T < 0 || T > kMaxDim) return fail(WQ_EINVAL, "T must be in 0..2^31-1 (got %lld)", (long long)T);
+  WQ_TRY(check_size(V, "V"));
   if (T == 0) return WQ_OK;
   WQ_PTR(ids);
   WQ_PTR(Wpacked);
@@ -425,7 +436,8 @@ wq_status wq_debug_route(int64_t M, int64_t N, int64_t K, int bits, int w4a8, in
     WQ_TRY(check_bits(bits));
   }
   WQ_TRY(check_group_k(128, K, "K"));
-  if (M < 1 || N < 1) return fail(WQ_EINVAL, "M and N must be >= 1");
+  WQ_TRY(check_size(M, "M"));
+  WQ_TRY(check_size(N, "N"));
   const Route r = w4a8 ? route_w4a8(M, N, K, sm_count) : route_wna16(M, N, K, bits, sm_count);
   *route = static_cast<int>(r);
   return WQ_OK;
@@ -436,7 +448,7 @@ wq_status wq_debug_unpack(const uint32_t* packed, int64_t N, int64_t K, int bits
   t_err[0] = 0;
   WQ_TRY(check_bits(bits));
   WQ_TRY(check_group_k(128, K, "K"));
-  if (N < 1) return fail(WQ_EINVAL, "N must be >= 1");
+  WQ_TRY(check_size(N, "N"));
   WQ_PTR(packed);
   WQ_PTR(codes);
   Ctx c{};
@@ -450,7 +462,8 @@ wq_status wq_debug_w4a8_group_acc(const int8_t* xq, int64_t M, const uint32_t* W
                                   int64_t K, int32_t* acc, void* stream) {
   t_err[0] = 0;
   WQ_TRY(check_group_k(128, K, "K"));
-  if (M < 1 || N < 1) return fail(WQ_EINVAL, "M and N must be >= 1");
+  WQ_TRY(check_size(M, "M"));
+  WQ_TRY(check_size(N, "N"));
   WQ_PTR(xq);
   WQ_PTR(Wpacked4);
   WQ_PTR(acc);
