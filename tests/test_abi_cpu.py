@@ -170,3 +170,28 @@ def test_host_tensors_are_refused(lib):
         wq.w4a8_gemm(x, torch.zeros(N, wq.packed_words_per_row(K, 4), dtype=torch.int32), scales, N, K)
     with pytest.raises(ValueError, match="CUDA tensor"):
         wq.qembed_gather(torch.zeros(2, dtype=torch.int32), packed, scales, N, K, bits)
+
+
+def test_device_failure_drops_cached_workspaces(lib):
+    """A call that failed on the device (launch error, or a timeout read by
+    check_status) may leave partial sums in a zero-at-rest workspace: the
+    binding forgets its cached buffers then. Argument errors launch nothing
+    and keep them."""
+    from weight_only_int2_gb300 import _lib as L
+
+    key = ("zero-at-rest", 0, 0)
+    try:
+        L._ws_cache[key] = object()
+        with pytest.raises(L.WQError):
+            L._check(L.WQ_ETIMEOUT, "wq_check_status")
+        assert key not in L._ws_cache
+        L._ws_cache[key] = object()
+        with pytest.raises(L.WQError):
+            L._check(L.WQ_ECUDA, "wna16_gemm")
+        assert key not in L._ws_cache
+        L._ws_cache[key] = object()
+        with pytest.raises(L.WQError):
+            L._check(L.WQ_EINVAL, "wna16_gemm")
+        assert key in L._ws_cache
+    finally:
+        L._ws_cache.pop(key, None)

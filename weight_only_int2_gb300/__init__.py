@@ -14,6 +14,7 @@ from ._lib import (  # noqa: F401
     debug_route,
     debug_unpack,
     debug_w4a8_group_acc,
+    drop_workspaces,
     load,
     packed_words_per_row,
     qembed_gather,

@@ -79,7 +79,13 @@ class WQError(RuntimeError):
 
 def _check(status: int, where: str) -> None:
     if status != WQ_OK:
-        raise WQError(status, where, load().wq_last_error().decode())
+        msg = load().wq_last_error().decode()
+        if status in (WQ_ECUDA, WQ_ETIMEOUT):
+            # device work may have stopped part-way: a zero-at-rest workspace
+            # can hold partial sums, so the cached buffers are dropped and the
+            # next call gets a zero-filled one (argument errors launch nothing)
+            drop_workspaces()
+        raise WQError(status, where, msg)
 
 
 def _ptr(t) -> int | None:
@@ -120,6 +126,14 @@ def _cached(kind: str, nbytes: int, device=None) -> torch.Tensor | None:
             buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=dev)
             _ws_cache[key] = buf
         return buf
+
+
+def drop_workspaces() -> None:
+    """Forgets every cached workspace and scratch buffer; later calls allocate
+    fresh zero-filled ones. Called after a device-side failure. The memory
+    returns to PyTorch's allocator, which reuses it in stream order."""
+    with _ws_lock:
+        _ws_cache.clear()
 
 
 def workspace(nbytes: int, device=None) -> torch.Tensor | None:
