@@ -101,7 +101,9 @@ size_t wna16_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits);
  *             tensor-core kernel needs none: 32 <= M <= 64 on a layer with a
  *             128-row tile for every two SMs);
  *             it must be zero-filled before its first use and every call that
- *             returns WQ_OK leaves it zero-filled again. Calls that may run
+ *             returns WQ_OK leaves it zero-filled again (a call that fails with
+ *             WQ_ECUDA, or whose kernel timed out as wq_check_status reports,
+ *             may leave partial sums: zero it before reuse). Calls that may run
  *             concurrently must not share one workspace. May be NULL when the
  *             required size is 0, or when the kernel the call takes uses none;
  *             a call whose kernel uses one returns WQ_EINVAL without it.
