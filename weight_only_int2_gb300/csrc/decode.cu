@@ -468,15 +468,10 @@ template <int B, int NT, int MODE>
 cudaError_t dlaunch(const Ctx& c, const CUtensorMap& wmap, const CUtensorMap& smap, const DParams& prm) {
   // Raise the per-device dynamic shared-memory opt-in when a launch needs more
   // than any earlier one did.
-  static size_t configured[64] = {};
-  if (c.device < 0 || c.device >= 64) return cudaErrorInvalidDevice;
+  static SmemLimit limit;
   const size_t smem = dsmem_bytes(B, NT, prm.gs, prm.sbox);
-  if (configured[c.device] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<B, NT, MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured[c.device] = smem;
-  }
+  const cudaError_t e = raise_smem_limit(limit, decode_kernel<B, NT, MODE>, c.device, smem);
+  if (e != cudaSuccess) return e;
   // Cooperative launch: the split-K finish waits on every CTA of the grid,
   // which is only safe when all of them are guaranteed to be resident.
   cudaLaunchConfig_t cfg{};

@@ -673,14 +673,10 @@ D2Plan make_d2plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
 
 template <int B, int NT, bool kQuant>
 cudaError_t d2launch(const Ctx& c, const CUtensorMap& wmap, const CUtensorMap& smap, const D2Plan& pl) {
-  static int configured[64] = {};  // dynamic smem opted in so far, per device
-  if (c.device < 0 || c.device >= 64) return cudaErrorInvalidDevice;
+  static SmemLimit limit;  // dynamic smem opted in so far, per device
   auto kern = decode2_kernel<B, NT, kQuant>;
-  if (configured[c.device] < static_cast<int>(pl.smem)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(pl.smem));
-    if (e != cudaSuccess) return e;
-    configured[c.device] = static_cast<int>(pl.smem);
-  }
+  const cudaError_t e = raise_smem_limit(limit, kern, c.device, pl.smem);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pl.prm.C), 1, 1);
   cfg.blockDim = dim3(kThreads2, 1, 1);

@@ -353,15 +353,10 @@ template <int B, int NT, int MODE>
 cudaError_t launch_t(const Ctx& c, const CUtensorMap& tmap, const Params& prm, const Plan& pl) {
   // The shared-memory opt-in is a per-device function attribute: raise it to
   // the largest size this instantiation can ask for, once per device.
-  static bool configured[64] = {};
-  if (c.device < 0 || c.device >= 64) return cudaErrorInvalidDevice;
-  if (!configured[c.device]) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<B, NT, MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes<B, NT>(kMaxGroupsPerCta)));
-    if (e != cudaSuccess) return e;
-    configured[c.device] = true;
-  }
+  static SmemLimit limit;
+  const cudaError_t e = raise_smem_limit(limit, gemv_kernel<B, NT, MODE>, c.device,
+                                         static_cast<size_t>(smem_bytes<B, NT>(kMaxGroupsPerCta)));
+  if (e != cudaSuccess) return e;
   const size_t smem = smem_bytes<B, NT>(pl.gper);
   const dim3 grid(pl.row_blocks, pl.splits, pl.mchunks);
   gemv_kernel<B, NT, MODE><<<grid, kThreads, smem, c.stream>>>(tmap, prm);

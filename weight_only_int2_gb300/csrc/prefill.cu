@@ -492,14 +492,9 @@ template <int B, int TN, bool kTok>
 cudaError_t plaunch(const Ctx& c, const CUtensorMap& xmap, const CUtensorMap& wmap, const PParams& prm) {
   constexpr size_t smem = Layout<B, TN>::kSmem;
   static_assert(smem <= 227 * 1024, "prefill stage layout exceeds shared memory");
-  static bool configured[64] = {};
-  if (c.device < 0 || c.device >= 64) return cudaErrorInvalidDevice;
-  if (!configured[c.device]) {
-    const cudaError_t e = cudaFuncSetAttribute(prefill_kernel<B, TN, kTok>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured[c.device] = true;
-  }
+  static SmemLimit limit;
+  const cudaError_t e = raise_smem_limit(limit, prefill_kernel<B, TN, kTok>, c.device, smem);
+  if (e != cudaSuccess) return e;
   PParams q = prm;
   q.row_tiles = static_cast<int>((prm.N + kBM - 1) / kBM);
   q.tok_tiles = static_cast<int>((prm.M + TN - 1) / TN);

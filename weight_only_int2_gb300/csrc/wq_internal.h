@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace wq {
 
 // Per-call launch context filled by the C-ABI layer.
@@ -18,6 +20,24 @@ struct Ctx {
 
 // Records a one-line error for wq_last_error() (thread-local).
 void set_error(const char* fmt, ...);
+
+// A kernel's dynamic shared-memory limit per device, raised on demand and
+// never lowered, under a lock: host threads that launch concurrently never
+// see a limit below the one they raised (a lowered limit would fail their
+// launch). One instance per kernel instantiation (a static in its launcher).
+struct SmemLimit {
+  std::mutex mu;
+  size_t bytes[64] = {};
+};
+template <typename Kernel>
+cudaError_t raise_smem_limit(SmemLimit& lim, Kernel kern, int device, size_t bytes) {
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(lim.mu);
+  if (lim.bytes[device] >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) lim.bytes[device] = bytes;
+  return e;
+}
 
 // Builds a 2-D tiled TMA descriptor over a row-major matrix of 32-bit words.
 // swizzle_bytes 0 (none), 32, 64 or 128: the shared-memory tile is written
