@@ -103,3 +103,21 @@ def test_shapes_no_kernel_takes():
     assert wq.debug_route(64, 17408, 28672, 6, SMS) == "tensor_core"
     assert wq.debug_route(100, 5120, 28672, 6, SMS) == "tensor_core"
     assert wq.debug_route(16, 8192, 28672, 6, SMS) == "decode_splitk"
+
+
+def test_zero_query_means_the_pair_kernel_on_every_device():
+    """The workspace query decides 'no workspace' for a few-token shape
+    without knowing the SM count: the pair plan's smallest configuration must
+    fit at min(N, 256) rows, at least the largest chunk any SM count gives. So
+    a zero query must mean the pair kernel at every SM count. (The converse
+    may fail where that bound is not reached, e.g. 257 rows give chunks of at
+    most 129: there the query is an upper bound, as documented.)"""
+    sms_list = (2, 3, 16, 76, 132, 148, 152, 160, 264)
+    for bits in range(2, 9):
+        for M in (1, 8, 9, 16):
+            for N in (1, 31, 32, 100, 256, 257, 5120, 17408, 248320):
+                for K in range(1024, 32768 + 1, 1024):
+                    zero = wq.wna16_workspace_bytes(M, N, K, bits) == 0
+                    routes = {wq.debug_route(M, N, K, bits, sms) for sms in sms_list}
+                    if zero:
+                        assert routes == {"decode_pair"}, (M, N, K, bits, routes)
