@@ -35,6 +35,7 @@ def _pin_calls():
              ("w4a8 vs wna16", P.test_w4a8_close_to_wna16_b4, ()),
              ("bf16 rne", P.test_bf16_rne_hand_cases, ()),
              ("gather -0.0", P.test_gather_negative_zero_and_unit_scale_b8, ()),
+             ("gather exact rounding", P.test_gather_exact_products_round_half_even, ()),
              ("page byte counts", P.test_page_byte_counts_pin_group_128_scales, ())]
     for b in range(2, 9):
         calls.append((f"round trip b{b}", P.test_round_trip_random_and_extremes, (b, 128)))
@@ -267,6 +268,9 @@ def _gather_variant(mode):
                 prod = (row_s * (qf - z)).astype(np.float32)
             if mode == "truncate":
                 out[t] = (np.ascontiguousarray(prod).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+            elif mode == "ties_away":       # round half away from zero
+                u = np.ascontiguousarray(prod).view(np.uint32).astype(np.uint64)
+                out[t] = ((u + np.uint64(0x8000)) >> np.uint64(16)).astype(np.uint16)
             else:
                 out[t] = W.f32_to_bf16_bits_rne(prod)
         return out, bad
@@ -301,6 +305,7 @@ MUTANTS = {
     "bf16 rounding half up": {"f32_to_bf16_bits_rne": _rne_half_up},
     "bf16 rounding by truncation": {"f32_to_bf16_bits_rne": _rne_truncate},
     "gather truncates to bf16": {"qembed_ref": _gather_variant("truncate")},
+    "gather rounds ties away from zero": {"qembed_ref": _gather_variant("ties_away")},
     "gather computes s*q - s*z": {"qembed_ref": _gather_variant("distributed")},
     "gather accepts id == V": {"qembed_ref": _gather_variant("id_bound")},
     "one scale per table row in the byte count": {"quantized_matrix_bytes": _bytes_scale_per_row},

@@ -354,6 +354,59 @@ def test_gather_is_rounded_dequant_with_ids_out_of_range(bits):
         assert np.all(np.abs(got - w[i]) <= np.abs(w[i]) * 2.0**-8)
 
 
+def _bf16_bits_of_rational(v: Fraction) -> int:
+    """bf16 bits of the rational v in the normal range, rounded to nearest
+    with ties to the even significand, from the format's definition (sign,
+    8-bit exponent with bias 127, 8 significant bits)."""
+    if v == 0:
+        return 0
+    sign = 0x8000 if v < 0 else 0
+    a, e = abs(v), 0
+    while a >= 2:
+        a, e = a / 2, e + 1
+    while a < 1:
+        a, e = a * 2, e - 1
+    m = _round_half_even(a * 128)          # 128..256
+    if m == 256:
+        m, e = 128, e + 1
+    return sign | ((e + 127) << 7) | (m - 128)
+
+
+def test_gather_exact_products_round_half_even():
+    """Every gathered element equals the exact product s * (q - z) rounded to
+    bf16 once, ties to even, computed in rationals. Scales 1 + k/128 (and
+    their negatives) against every 8-bit code give products with 9 to 16
+    significant bits, many exactly halfway between two bf16 values, with both
+    neighbours' parities."""
+    bits, z = 8, 128
+    scales_bits = [0x3F80 + k for k in range(1, 16)] + [0xBF80 + k for k in range(1, 16)]
+    rows, srows = [], []
+    for sb in scales_bits:
+        rows += [list(range(0, 128)), list(range(128, 256))]
+        srows += [[sb], [sb]]
+    q = np.array(rows, dtype=np.int64)                     # V = 60 rows, D = 128
+    s = np.array(srows, dtype=np.uint16)
+    out, bad = O.qembed_ref(np.arange(len(rows)), q, s, bits)
+    assert bad == 0
+    ties = {0: 0, 1: 0}
+    for r in range(len(rows)):
+        sv = _frac_bf16(s[r, 0])
+        for d in range(128):
+            v = sv * (int(q[r, d]) - z)
+            if v != 0:
+                a = abs(v)
+                while a >= 2:
+                    a /= 2
+                while a < 1:
+                    a *= 2
+                t = a * 128
+                if t - int(t) == Fraction(1, 2):
+                    ties[int(t) % 2] += 1
+            want = _bf16_bits_of_rational(v) if v != 0 else (0x8000 if sv < 0 else 0)
+            assert int(out[r, d]) == want, (r, d)
+    assert ties[0] > 0 and ties[1] > 0, ties
+
+
 def test_gather_negative_zero_and_unit_scale_b8():
     q = np.array([[128] * 128 + [0] * 128], dtype=np.int64)   # V=1, D=256
     s = np.array([[0xBF80, 0x3F80]], dtype=np.uint16)         # -1.0, +1.0
