@@ -128,6 +128,9 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
  *    return WQ_EINVAL with a message, unless they run on the tensor-core
  *    kernel, which needs no scratch (32 <= M <= 64 on a layer with a
  *    128-row tile for every two SMs); use wna16_gemm for the others.
+ *  - Every argument check of wna16_gemm runs first: a call with bad
+ *    arguments returns WQ_EINVAL (or WQ_EUNSUPPORTED) with nothing enqueued
+ *    and the array untouched.
  *  - The scratch region used is cleared on `stream` before the GEMM, so no
  *    state carries over between calls; calls whose executions overlap on the
  *    GPU (other streams, other host threads) share the array and race.
@@ -219,6 +222,13 @@ wq_status wq_debug_unpack(const uint32_t* packed, int64_t N, int64_t K, int bits
  * w4a8_gemm, acc [M, N, K/128] int32 output. */
 wq_status wq_debug_w4a8_group_acc(const int8_t* xq, int64_t M, const uint32_t* Wpacked4,
                                   int64_t N, int64_t K, int32_t* acc, void* stream);
+
+/* Copies `bytes` (at most 4 MiB) between the caller's device buffer `buf` and
+ * the start of wna16_gemm_noalloc's scratch array on the current device
+ * (to_scratch = 1: buf -> scratch; 0: scratch -> buf), asynchronously on
+ * `stream`. For tests that plant a sentinel in the array or read it back.
+ * Like wna16_gemm_noalloc, it has no counterpart on the source pages. */
+wq_status wq_debug_noalloc_scratch(void* buf, size_t bytes, int to_scratch, void* stream);
 
 /* Reads and clears the status word of the current device (synchronizes the
  * device). Returns WQ_OK, WQ_ETIMEOUT if a kernel gave up on a pipeline wait,

@@ -51,3 +51,34 @@ def assert_bf16_close(y_dev, y_ref, what=""):
     fro, mx = errors(bf16_dev_to_f64(y_dev), y_ref)
     assert fro <= REL_FRO and mx <= REL_MAX, f"{what}: rel_fro={fro:.3e} rel_max={mx:.3e}"
     return fro, mx
+
+
+class Guarded:
+    """A device output tensor placed between two sentinel bands of a larger
+    buffer (the stand-in for an out-of-bounds checker): after the call,
+    check() asserts that no byte of either band changed. The tensor itself is
+    pre-filled with the same pattern, so elements a kernel never writes also
+    stand out against the oracle."""
+
+    BAND = 4096
+    PATTERN = 0xA5
+
+    def __init__(self, shape, dtype):
+        import torch
+
+        self.shape = tuple(int(d) for d in shape)
+        item = torch.empty((), dtype=dtype).element_size()
+        self.nbytes = int(np.prod(self.shape, dtype=np.int64)) * item
+        body = (self.nbytes + 15) // 16 * 16
+        self.raw = torch.full((self.BAND + body + self.BAND,), self.PATTERN, dtype=torch.uint8, device="cuda")
+        self.t = self.raw[self.BAND:self.BAND + self.nbytes].view(dtype).view(self.shape)
+
+    def check(self, what=""):
+        import torch
+
+        torch.cuda.synchronize()
+        lo = self.raw[:self.BAND]
+        hi = self.raw[self.BAND + self.nbytes:]
+        bad_lo = int((lo != self.PATTERN).sum())
+        bad_hi = int((hi != self.PATTERN).sum())
+        assert bad_lo == 0 and bad_hi == 0, f"{what}: {bad_lo} bytes before and {bad_hi} after the output changed"

@@ -69,8 +69,27 @@ def test_workspace_sizes(lib):
     assert lib.w4a8_scratch_bytes(8, 256) >= 8 * 256 + 8 * 4
 
 
-def test_bad_arguments_rejected_before_any_cuda_call(lib):
-    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: validation fails first
+@pytest.fixture(scope="module")
+def fake():
+    """A pointer that the checks below never let a kernel use. Without a GPU
+    it is a plain address (no CUDA call can touch it); where a GPU is present
+    it is a real 64 MiB device buffer, so that a regression that launched a
+    kernel would still touch valid memory of the right sizes."""
+    try:
+        import torch
+
+        if torch.cuda.is_available():
+            buf = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
+            yield ctypes.c_void_p(buf.data_ptr())
+            torch.cuda.synchronize()
+            return
+    except ImportError:  # pragma: no cover
+        pass
+    yield ctypes.c_void_p(1 << 20)
+
+
+def test_bad_arguments_rejected_before_any_cuda_call(lib, fake):
+    addr = fake.value
     # bits out of range
     assert lib.wna16_gemm(fake, 1, fake, fake, 8, 128, 9, 128, fake, None, 0, None) == 1
     assert b"bits" in lib.wq_last_error()
@@ -80,7 +99,7 @@ def test_bad_arguments_rejected_before_any_cuda_call(lib):
     assert lib.wna16_repack(fake, fake, 4, 100, 6, 128, fake, fake, None, None) == 1
     # null pointers and misalignment
     assert lib.wna16_gemm(None, 1, fake, fake, 8, 128, 6, 128, fake, None, 0, None) == 1
-    assert lib.wna16_gemm(ctypes.c_void_p((1 << 20) + 2), 1, fake, fake, 8, 128, 6, 128, fake, None, 0,
+    assert lib.wna16_gemm(ctypes.c_void_p(addr + 2), 1, fake, fake, 8, 128, 6, 128, fake, None, 0,
                           None) == 1
     assert b"aligned" in lib.wq_last_error()
     # M = 0

@@ -7,7 +7,7 @@ import pytest
 
 import oracle as O
 import wq_inputs as I
-from helpers import (assert_bf16_close, bf16_dev_to_bits, packed_dev_to_u32, to_dev,
+from helpers import (Guarded, assert_bf16_close, bf16_dev_to_bits, packed_dev_to_u32, to_dev,
                      to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
@@ -36,8 +36,11 @@ def test_repack_bit_exact(bits, N, K):
     q[-1, -5:] = 0
     bad = torch.zeros(1, dtype=torch.int32, device="cuda")
     s = I.make_scales(N, K // 128, 7)
-    packed, s_out = wq.wna16_repack(to_dev(q), to_dev_bf16(s), bits, bad_count=bad)
-    torch.cuda.synchronize()
+    gp = Guarded((N, wq.packed_words_per_row(K, bits)), torch.int32)
+    gs = Guarded((N, K // 128), torch.bfloat16)
+    packed, s_out = wq.wna16_repack(to_dev(q), to_dev_bf16(s), bits, packed=gp.t, scales_out=gs.t, bad_count=bad)
+    gp.check("packed")
+    gs.check("scales_out")
     assert np.array_equal(packed_dev_to_u32(packed), O.pack(q, bits))
     assert np.array_equal(bf16_dev_to_bits(s_out), s)
     assert int(bad.item()) == 0
@@ -102,8 +105,9 @@ def test_wna16_gemm_matches_oracle(M, N, K, bits):
     seed = 10 * M + N + bits
     x = I.make_x(M, K, seed)
     q, s, packed, s_dev = _layer(N, K, bits, seed + 3)
-    y = wq.wna16_gemm(to_dev_bf16(x), packed, s_dev, N, K, bits)
-    torch.cuda.synchronize()
+    g = Guarded((M, N), torch.bfloat16)
+    y = wq.wna16_gemm(to_dev_bf16(x), packed, s_dev, N, K, bits, y=g.t)
+    g.check(f"y M={M} N={N} K={K} b={bits}")
     assert_bf16_close(y, O.wna16_ref(x, q, s, bits), f"M={M} N={N} K={K} b={bits}")
 
 
@@ -149,8 +153,10 @@ def test_act_quant_bit_exact(M, K):
     x = I.make_x_outliers(M, K, M + K)
     if M > 2:
         x[1] = 0
-    xq, sx = wq.act_quant_int8(to_dev_bf16(x))
-    torch.cuda.synchronize()
+    gq, gs = Guarded((M, K), torch.int8), Guarded((M,), torch.float32)
+    xq, sx = wq.act_quant_int8(to_dev_bf16(x), xq=gq.t, sx=gs.t)
+    gq.check("xq")
+    gs.check("sx")
     rq, rs = O.act_quant_ref(x)
     assert np.array_equal(xq.cpu().numpy(), rq)
     assert np.array_equal(sx.cpu().numpy().view(np.uint32), rs.view(np.uint32))
@@ -184,8 +190,9 @@ def test_w4a8_group_accumulators_bit_exact(M, N, K):
 def test_w4a8_gemm_matches_oracle(M, N, K, sign):
     x = I.make_x_outliers(M, K, 20 + M)
     q, s, packed, s_dev = _layer(N, K, 4, 21 + M, sign=sign)
-    y = wq.w4a8_gemm(to_dev_bf16(x), packed, s_dev, N, K)
-    torch.cuda.synchronize()
+    g = Guarded((M, N), torch.bfloat16)
+    y = wq.w4a8_gemm(to_dev_bf16(x), packed, s_dev, N, K, y=g.t)
+    g.check(f"w4a8 y M={M}")
     y_ref, _, _ = O.w4a8_ref(x, q, s)
     assert_bf16_close(y, y_ref, f"w4a8 M={M}")
 
@@ -205,8 +212,9 @@ def test_gather_bit_exact(bits):
     ids[6] = V
     packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(s), bits)
     bad = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = wq.qembed_gather(to_dev(ids), packed, s_dev, V, D, bits, bad_count=bad)
-    torch.cuda.synchronize()
+    g = Guarded((T, D), torch.bfloat16)
+    out = wq.qembed_gather(to_dev(ids), packed, s_dev, V, D, bits, out=g.t, bad_count=bad)
+    g.check("gather out")
     ref, nbad = O.qembed_ref(ids, q, s, bits)
     assert np.array_equal(bf16_dev_to_bits(out), ref)
     assert int(bad.item()) == nbad == 2
@@ -223,8 +231,9 @@ def test_gather_long_rows(bits):
     ids = np.array([4, 0, 2, 2, -1, 3, 1], dtype=np.int32)
     packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(s), bits)
     bad = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = wq.qembed_gather(to_dev(ids), packed, s_dev, V, D, bits, bad_count=bad)
-    torch.cuda.synchronize()
+    g = Guarded((T, D), torch.bfloat16)
+    out = wq.qembed_gather(to_dev(ids), packed, s_dev, V, D, bits, out=g.t, bad_count=bad)
+    g.check("gather out (long rows)")
     ref, nbad = O.qembed_ref(ids, q, s, bits)
     assert np.array_equal(bf16_dev_to_bits(out), ref)
     assert int(bad.item()) == nbad == 1

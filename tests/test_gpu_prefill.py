@@ -11,7 +11,7 @@ import pytest
 
 import oracle as O
 import wq_inputs as I
-from helpers import assert_bf16_close, to_dev, to_dev_bf16
+from helpers import Guarded, assert_bf16_close, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -49,8 +49,9 @@ def test_prefill_matches_oracle(M, N, K, bits):
     seed = 7 * M + N + bits
     x = I.make_x(M, K, seed)
     q, s, packed, s_dev = _layer(N, K, bits, seed + 5)
-    y = wq.wna16_gemm(to_dev_bf16(x), packed, s_dev, N, K, bits)
-    torch.cuda.synchronize()
+    g = Guarded((M, N), torch.bfloat16)
+    y = wq.wna16_gemm(to_dev_bf16(x), packed, s_dev, N, K, bits, y=g.t)
+    g.check(f"y M={M} N={N} K={K} b={bits}")
     assert_bf16_close(y, O.wna16_ref(x, q, s, bits), f"M={M} N={N} K={K} b={bits}")
 
 
@@ -92,25 +93,30 @@ def test_prefill_needs_no_workspace():
 def test_w4a8_prefill_matches_oracle(M, N, K, sign):
     x = I.make_x_outliers(M, K, 90 + M)
     q, s, packed, s_dev = _layer(N, K, 4, 91 + M, sign=sign)
-    y = wq.w4a8_gemm(to_dev_bf16(x), packed, s_dev, N, K)
-    torch.cuda.synchronize()
+    g = Guarded((M, N), torch.bfloat16)
+    y = wq.w4a8_gemm(to_dev_bf16(x), packed, s_dev, N, K, y=g.t)
+    g.check(f"w4a8 y M={M}")
     y_ref, _, _ = O.w4a8_ref(x, q, s)
     assert_bf16_close(y, y_ref, f"w4a8 prefill M={M}")
 
 
-def test_prefill_full_size_sampled():
-    """M=8192, N=17408, K=5120, 6-bit: the prefill configuration. The oracle
-    computes 48 token rows x 48 weight rows drawn over the whole output."""
-    M, N, K, bits = 8192, 17408, 5120, 6
-    x = I.make_x(M, K, 8192)
-    q = I.make_codes(N, K, bits, 8193)
-    s = I.make_scales(N, K // 128, 8194)
+@pytest.mark.parametrize("M,bits", [(8192, 5), (8192, 6), (8192, 7), (8192, 8), (2048, 5), (2048, 6),
+                                    (2048, 7), (2048, 8)])
+def test_prefill_full_size_sampled(M, bits):
+    """N=17408, K=5120 at every width and both token counts of the prefill
+    configuration. The oracle computes 48 token rows x 48 weight rows drawn
+    over the whole output."""
+    N, K = 17408, 5120
+    x = I.make_x(M, K, 8192 + M)
+    q = I.make_codes(N, K, bits, 8193 + bits)
+    s = I.make_scales(N, K // 128, 8194 + bits)
     packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(s), bits)
-    y = wq.wna16_gemm(to_dev_bf16(x), packed, s_dev, N, K, bits)
-    torch.cuda.synchronize()
-    r = np.random.default_rng(5)
+    g = Guarded((M, N), torch.bfloat16)
+    y = wq.wna16_gemm(to_dev_bf16(x), packed, s_dev, N, K, bits, y=g.t)
+    g.check(f"full-size y M={M} b={bits}")
+    r = np.random.default_rng(5 + bits)
     ms = np.unique(np.concatenate([r.choice(M, 46, replace=False), [0, M - 1]]))
     ns = np.unique(np.concatenate([r.choice(N, 46, replace=False), [0, N - 1]]))
     got = y[torch.as_tensor(ms, device="cuda")][:, torch.as_tensor(ns, device="cuda")]
     ref = O.wna16_ref(x[ms], q[ns], s[ns], bits)
-    assert_bf16_close(got, ref, "full-size sampled")
+    assert_bf16_close(got, ref, f"full-size sampled M={M} b={bits}")

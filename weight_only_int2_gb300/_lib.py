@@ -44,6 +44,7 @@ SIGNATURES = {
     "wq_debug_route": (_c_int, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_ptr]),
     "wq_debug_unpack": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr]),
     "wq_debug_w4a8_group_acc": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr]),
+    "wq_debug_noalloc_scratch": (_c_int, [_c_ptr, _c_size, _c_int, _c_ptr]),
     "wq_check_status": (_c_int, []),
     "wq_last_error": (ctypes.c_char_p, []),
     "wq_version": (ctypes.c_char_p, []),

@@ -115,12 +115,6 @@ wq_status no_route(int64_t M, int64_t N, int64_t K) {
               (long long)M, (long long)N, (long long)K);
 }
 
-// A 32..64-token shape that the tensor-core kernel may take (decided with the
-// SM count): its workspace is checked only if the route turns out to use it.
-bool maybe_tensor_core(int64_t M, int64_t N, int64_t K, int bits) {
-  return M >= 32 && M < kPrefillMinTokens && prefill_supported(M, N, K, bits);
-}
-
 #define WQ_TRY(expr)            \
   do {                          \
     wq_status _s = (expr);      \
@@ -140,6 +134,49 @@ void set_error(const char* fmt, ...) {
   va_start(ap, fmt);
   vsnprintf(t_err, sizeof(t_err), fmt, ap);
   va_end(ap);
+}
+
+wq_status wna16_check_args(const uint16_t* x, int64_t M, const uint32_t* Wpacked, const uint16_t* scales,
+                           int64_t N, int64_t K, int bits, int group, const uint16_t* y) {
+  WQ_TRY(check_bits(bits));
+  WQ_TRY(check_group_k(group, K, "K"));
+  WQ_TRY(check_size(M, "M"));
+  WQ_TRY(check_size(N, "N"));
+  WQ_PTR(x);
+  WQ_PTR(Wpacked);
+  WQ_PTR(scales);
+  WQ_PTR(y);
+  return WQ_OK;
+}
+
+bool maybe_tensor_core(int64_t M, int64_t N, int64_t K, int bits) {
+  return M >= 32 && M < kPrefillMinTokens && prefill_supported(M, N, K, bits);
+}
+
+wq_status wna16_route(int64_t M, int64_t N, int64_t K, int bits, void* stream, Ctx* c, Route* r) {
+  WQ_TRY(get_ctx(stream, c));
+  *r = route_wna16(M, N, K, bits, c->sm_count);
+  if (*r == Route::kNone) return no_route(M, N, K);
+  return WQ_OK;
+}
+
+wq_status wna16_launch(const Ctx& c, Route r, const uint16_t* x, int64_t M, const uint32_t* Wpacked,
+                       const uint16_t* scales, int64_t N, int64_t K, int bits, uint16_t* y, void* workspace) {
+  GemvArgs a{};
+  a.mode = GemvMode::kWna16;
+  a.x = x;
+  a.packed = Wpacked;
+  a.scales = scales;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.bits = bits;
+  a.y = y;
+  a.ws = static_cast<float*>(workspace);
+  cudaError_t e = r == Route::kTensorCore ? launch_prefill(c, x, Wpacked, scales, M, N, K, bits, y, nullptr)
+                                          : launch_routed(c, r, a);
+  if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "wna16_gemm launch");
+  return WQ_OK;
 }
 
 static bool ensure_encode() {
@@ -266,40 +303,18 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
                      int64_t N, int64_t K, int bits, int group, wq_bf16* y, void* workspace,
                      size_t ws_bytes, void* stream) {
   t_err[0] = 0;
-  WQ_TRY(check_bits(bits));
-  WQ_TRY(check_group_k(group, K, "K"));
-  WQ_TRY(check_size(M, "M"));
-  WQ_TRY(check_size(N, "N"));
-  WQ_PTR(x);
-  WQ_PTR(Wpacked);
-  WQ_PTR(scales);
-  WQ_PTR(y);
+  WQ_TRY(wna16_check_args(x, M, Wpacked, scales, N, K, bits, group, y));
   // The documented size is checked before any device call, except for a
   // 32..64-token shape the tensor-core GEMM may take (known from the SM
   // count); then the route's own need, whatever the query said.
   const size_t need = stream_workspace_bytes(M, N, K, bits);
   if (need > 0 && !maybe_tensor_core(M, N, K, bits)) WQ_TRY(check_workspace(workspace, ws_bytes, need));
   Ctx c{};
-  WQ_TRY(get_ctx(stream, &c));
-  const Route r = route_wna16(M, N, K, bits, c.sm_count);
-  if (r == Route::kNone) return no_route(M, N, K);
+  Route r = Route::kNone;
+  WQ_TRY(wna16_route(M, N, K, bits, stream, &c, &r));
   const size_t need_r = route_workspace_bytes(r, M, N, K);
   if (need_r > 0) WQ_TRY(check_workspace(workspace, ws_bytes, need_r));
-  GemvArgs a{};
-  a.mode = GemvMode::kWna16;
-  a.x = x;
-  a.packed = Wpacked;
-  a.scales = scales;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.bits = bits;
-  a.y = y;
-  a.ws = static_cast<float*>(workspace);
-  cudaError_t e = r == Route::kTensorCore ? launch_prefill(c, x, Wpacked, scales, M, N, K, bits, y, nullptr)
-                                          : launch_routed(c, r, a);
-  if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "wna16_gemm launch");
-  return WQ_OK;
+  return wna16_launch(c, r, x, M, Wpacked, scales, N, K, bits, y, workspace);
 }
 
 wq_status act_quant_int8(const wq_bf16* x, int64_t M, int64_t K, int8_t* xq, float* sx,

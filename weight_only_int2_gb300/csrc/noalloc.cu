@@ -15,6 +15,10 @@
 // Its first use on a device resolves the array's device address with
 // cudaGetSymbolAddress (the array's name is only a host-side stand-in); that
 // first call should therefore come before any stream capture.
+//
+// Order of a call: every argument check of wna16_gemm first (nothing is
+// enqueued for a call that fails them), then the route and its scratch need,
+// then the clearing of that region and the GEMM, both on the caller's stream.
 #include "wq.h"
 #include "wq_device.cuh"
 #include "wq_internal.h"
@@ -32,6 +36,34 @@ constexpr int kMaxDev = 64;
 void* g_scratch_ptr[kMaxDev] = {};
 std::mutex g_scratch_mu;
 
+wq_status too_big(size_t need) {
+  set_error("wna16_gemm_noalloc: this shape needs %zu bytes of scratch, above the fixed %zu-byte array "
+            "(use wna16_gemm with a caller-provided workspace)",
+            need, kNoAllocScratchBytes);
+  return WQ_EINVAL;
+}
+
+// The device address of the scratch array on device `dev` (current), looked
+// up once per device with that device current.
+wq_status scratch_address(int dev, void** out) {
+  if (dev < 0 || dev >= kMaxDev) {
+    set_error("wna16_gemm_noalloc: device index %d too large", dev);
+    return WQ_EUNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      set_error("wna16_gemm_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      return WQ_ECUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return WQ_OK;
+}
+
 }  // namespace
 }  // namespace wq
 
@@ -40,67 +72,58 @@ using namespace wq;
 extern "C" wq_status wna16_gemm_noalloc(const wq_bf16* x, int64_t M, const uint32_t* Wpacked,
                                         const wq_bf16* scales, int64_t N, int64_t K, int bits, int group,
                                         wq_bf16* y, void* stream) {
-  // The same argument checks as wna16_gemm, plus the scratch limit. A
-  // 32..64-token shape that the tensor-core kernel takes needs no scratch;
-  // that is known once the device's SM count is.
-  size_t need = wna16_workspace_bytes(M, N, K, bits);
-  const bool maybe_tc = M >= 32 && M < kPrefillMinTokens && bits >= 2 && bits <= 8 && group == 128 &&
-                        prefill_supported(M, N, K, bits);
-  if (need > kNoAllocScratchBytes && !maybe_tc) {
-    set_error("wna16_gemm_noalloc: this shape needs %zu bytes of scratch, above the fixed %zu-byte array "
-              "(use wna16_gemm with a caller-provided workspace)",
-              need, kNoAllocScratchBytes);
-    return WQ_EINVAL;
-  }
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    set_error("wna16_gemm_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
-    return WQ_ECUDA;
-  }
-  if (maybe_tc) {
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) {
-      set_error("wna16_gemm_noalloc: SM count: %s", cudaGetErrorString(e));
-      return WQ_ECUDA;
-    }
-    if (route_wna16(M, N, K, bits, sms) == Route::kTensorCore) need = 0;
-    if (need > kNoAllocScratchBytes) {
-      set_error("wna16_gemm_noalloc: this shape needs %zu bytes of scratch, above the fixed %zu-byte array "
-                "(use wna16_gemm with a caller-provided workspace)",
-                need, kNoAllocScratchBytes);
-      return WQ_EINVAL;
-    }
-  }
-  if (dev < 0 || dev >= kMaxDev) {
-    set_error("wna16_gemm_noalloc: device index %d too large", dev);
-    return WQ_EUNSUPPORTED;
-  }
+  set_error("");
+  // 1. The argument checks of wna16_gemm, before anything touches the device.
+  wq_status st = wna16_check_args(x, M, Wpacked, scales, N, K, bits, group, y);
+  if (st != WQ_OK) return st;
+  // 2. The scratch limit: the documented need when it is known without the
+  //    device, else (32..64 tokens, where the tensor-core kernel may take the
+  //    shape) the need of the route the device picks.
+  const size_t need_q = wna16_workspace_bytes(M, N, K, bits);
+  if (need_q > kNoAllocScratchBytes && !maybe_tensor_core(M, N, K, bits)) return too_big(need_q);
+  Ctx c{};
+  Route r = Route::kNone;
+  st = wna16_route(M, N, K, bits, stream, &c, &r);
+  if (st != WQ_OK) return st;
+  const size_t need = route_workspace_bytes(r, M, N, K);
+  if (need > kNoAllocScratchBytes) return too_big(need);
+  // 3. Clear the region the route uses (the split-K partials and counters
+  //    must start at zero), then run the GEMM on it, both on `stream`.
   void* ptr = nullptr;
-  {
-    // Set-up, once per device with that device current: the device address of
-    // the scratch array (a kernel given the host-side symbol would fault).
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-      if (e != cudaSuccess || p == nullptr) {
-        set_error("wna16_gemm_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        return WQ_ECUDA;
-      }
-      g_scratch_ptr[dev] = p;
-    }
-    ptr = g_scratch_ptr[dev];
-  }
   if (need > 0) {
-    // The split-K region must start at zero; clear it rather than rely on the
-    // contents left by the previous call.
-    e = cudaMemsetAsync(ptr, 0, need, static_cast<cudaStream_t>(stream));
+    st = scratch_address(c.device, &ptr);
+    if (st != WQ_OK) return st;
+    const cudaError_t e = cudaMemsetAsync(ptr, 0, need, c.stream);
     if (e != cudaSuccess) {
       set_error("wna16_gemm_noalloc: clearing the scratch: %s", cudaGetErrorString(e));
       return WQ_ECUDA;
     }
   }
-  return wna16_gemm(x, M, Wpacked, scales, N, K, bits, group, y, need > 0 ? ptr : nullptr, need, stream);
+  return wna16_launch(c, r, x, M, Wpacked, scales, N, K, bits, y, ptr);
+}
+
+extern "C" wq_status wq_debug_noalloc_scratch(void* buf, size_t bytes, int to_scratch, void* stream) {
+  set_error("");
+  if (buf == nullptr || (to_scratch != 0 && to_scratch != 1) || bytes > kNoAllocScratchBytes) {
+    set_error("wq_debug_noalloc_scratch: buf must be non-NULL, to_scratch 0 or 1, bytes <= %zu",
+              kNoAllocScratchBytes);
+    return WQ_EINVAL;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error("wq_debug_noalloc_scratch: cudaGetDevice: %s", cudaGetErrorString(e));
+    return WQ_ECUDA;
+  }
+  void* ptr = nullptr;
+  const wq_status st = scratch_address(dev, &ptr);
+  if (st != WQ_OK) return st;
+  if (bytes == 0) return WQ_OK;
+  e = to_scratch ? cudaMemcpyAsync(ptr, buf, bytes, cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream))
+                 : cudaMemcpyAsync(buf, ptr, bytes, cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    set_error("wq_debug_noalloc_scratch: copy: %s", cudaGetErrorString(e));
+    return WQ_ECUDA;
+  }
+  return WQ_OK;
 }

@@ -8,6 +8,8 @@
 
 #include <mutex>
 
+#include "wq.h"
+
 namespace wq {
 
 // Per-call launch context filled by the C-ABI layer.
@@ -204,5 +206,22 @@ inline size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits) 
   const size_t a = gemv_workspace_bytes(M, N, K), b = decode_workspace_bytes(M, N);
   return a > b ? a : b;
 }
+
+// ---- the WNA16 entry point in steps (api.cu), shared by wna16_gemm and the
+// allocation-free variant so that both validate and route identically ----
+
+// Every argument check that needs no device call (bits, group, sizes,
+// pointers); records the message and returns WQ_EINVAL/WQ_EUNSUPPORTED.
+wq_status wna16_check_args(const uint16_t* x, int64_t M, const uint32_t* Wpacked, const uint16_t* scales, int64_t N,
+                     int64_t K, int bits, int group, const uint16_t* y);
+// A 32..64-token shape that the tensor-core kernel may take (decided with the
+// SM count): its workspace is checked only if the route turns out to use it.
+bool maybe_tensor_core(int64_t M, int64_t N, int64_t K, int bits);
+// The device context and the kernel the shape takes (device queries, no
+// launch); WQ_EUNSUPPORTED when no kernel takes it.
+wq_status wna16_route(int64_t M, int64_t N, int64_t K, int bits, void* stream, Ctx* c, Route* r);
+// Launches route r (arguments already checked; workspace as the route needs).
+wq_status wna16_launch(const Ctx& c, Route r, const uint16_t* x, int64_t M, const uint32_t* Wpacked,
+                 const uint16_t* scales, int64_t N, int64_t K, int bits, uint16_t* y, void* workspace);
 
 }  // namespace wq
