@@ -163,7 +163,11 @@ size_t w4a8_scratch_bytes(int64_t M, int64_t K);
  * and K % 1024 == 0 inside the decode kernel, same arithmetic), then with
  * int4 codes q and zero point 8,
  *   acc[m, n, g] = sum_{k in group g} xq[m, k] * (q[n, k] - 8)   (exact, int32)
- *   y[m, n] = bf16( sx[m] * sum_g s[n, g] * acc[m, n, g] ).
+ *   y[m, n] = bf16( sx[m] * sum_g s[n, g] * acc[m, n, g] ),
+ * the group sum in float32 over g in order. Every route computes each
+ * acc[m, n, g] exactly (integer-valued products and sums below 2^24 on the
+ * tensor cores, one accumulator per group) before applying s[n, g];
+ * wq_debug_w4a8_group_acc returns them.
  *  Wpacked4 [N, K/8] uint32 (v1 layout, bits = 4); scales [N, K/128] bf16.
  *  workspace, ws_bytes: at least w4a8_workspace_bytes(); zero-fill and NULL
  *             contract as for wna16_gemm.
@@ -217,11 +221,15 @@ wq_status wq_debug_unpack(const uint32_t* packed, int64_t N, int64_t K, int bits
                           uint8_t* codes, void* stream);
 
 /* The exact per-group integer accumulators of the W4A8 main loop [W4A8]:
- *   acc[m, n, g] = sum_{k in group g} xq[m, k] * (q[n, k] - 8)
- * computed by the same kernel as w4a8_gemm. xq [M, K] int8, Wpacked4 as in
- * w4a8_gemm, acc [M, N, K/128] int32 output. */
-wq_status wq_debug_w4a8_group_acc(const int8_t* xq, int64_t M, const uint32_t* Wpacked4,
-                                  int64_t N, int64_t K, int32_t* acc, void* stream);
+ *   acc[m, n, g] = sum_{k in group g} xq[m, k] * (q[n, k] - 8),
+ * with xq = act_quant_int8(x), computed by the kernel that w4a8_gemm launches
+ * for the same shape (same route, same quantization of x, same main loop),
+ * which writes these int32 sums instead of y. Arguments as w4a8_gemm, with
+ * acc [M, N, K/128] int32 in place of y and no workspace (the accumulators
+ * need no split-K partials). */
+wq_status wq_debug_w4a8_group_acc(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4,
+                                  const wq_bf16* scales, int64_t N, int64_t K, int32_t* acc,
+                                  void* scratch, size_t scratch_bytes, void* stream);
 
 /* Copies `bytes` (at most 4 MiB) between the caller's device buffer `buf` and
  * the start of wna16_gemm_noalloc's scratch array on the current device

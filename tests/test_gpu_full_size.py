@@ -104,6 +104,28 @@ def test_w4a8_full_size(M):
     assert_bf16_close(got, y_ref, f"w4a8 M={M}")
 
 
+def test_w4a8_group_accumulators_full_size_sampled():
+    """The exact int32 group accumulators at the full W4A8 prefill size
+    (8192 x 17408 x 5120, the tensor-core route), sampled: every entry
+    acc[m, n, g] depends only on token m and weight row n."""
+    M, N = 8192, 17408
+    G = K // 128
+    assert wq.debug_route(M, N, K, 4, torch.cuda.get_device_properties(0).multi_processor_count,
+                          w4a8=True) == "tensor_core"
+    q = I.make_codes(N, K, 4, 2400)
+    packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(I.make_scales(N, G, 2401)), 4)
+    x = I.make_x_outliers(M, K, 2402)
+    acc = wq.debug_w4a8_group_acc(to_dev_bf16(x), packed, s_dev, N, K)   # 22.8 GB of int32
+    torch.cuda.synchronize()
+    ms = _sample(M, 24, 12, must=[0, M - 1])
+    ns = _sample(N, 64, 13, must=[0, N - 1])
+    got = acc[torch.as_tensor(ms, device="cuda")][:, torch.as_tensor(ns, device="cuda")].cpu().numpy()
+    del acc
+    xq_ref, _ = O.act_quant_ref(x[ms])                                   # per token: rows are independent
+    assert np.array_equal(got.astype(np.int64), O.w4a8_group_acc(xq_ref, q[ns]))
+    wq.check_status()
+
+
 def _stack_bits(layer):
     """Layers 0-9 and 54-63: 7 bits; 10-53 alternate 5 / 6, starting with 5."""
     if layer < 10 or layer >= 54:

@@ -172,15 +172,29 @@ def test_act_quant_half_way_cases():
 
 # ------------------------------------------------------------------ W4A8
 
-@pytest.mark.parametrize("M,N,K", [(1, 100, 256), (5, 257, 640), (16, 128, 1280), (70, 90, 384),
-                                   (1, 300, 1024), (16, 200, 2048), (7, 64, 5120)])
-def test_w4a8_group_accumulators_bit_exact(M, N, K):
+# (M, N, K, route): the debug entry runs the kernel w4a8_gemm launches for the
+# shape, so every route's integer accumulators are checked bit for bit
+W4A8_ACC_CASES = [
+    (1, 100, 256, "chunked"), (5, 257, 640, "chunked"), (16, 128, 1280, "chunked"),
+    (1, 300, 1024, "decode_pair"), (16, 200, 2048, "decode_pair"), (7, 64, 5120, "decode_pair"),
+    (1, 1000, 5120, "decode_pair"), (16, 333, 2048, "decode_pair"),
+    (16, 700, 14336, "decode_splitk"),
+    (70, 90, 384, "tensor_core"), (100, 257, 640, "tensor_core"), (129, 300, 1024, "tensor_core"),
+    (512, 640, 5120, "tensor_core"), (1000, 130, 256, "tensor_core"),
+]
+
+
+@pytest.mark.parametrize("M,N,K,route", W4A8_ACC_CASES)
+def test_w4a8_group_accumulators_bit_exact(M, N, K, route):
+    assert wq.debug_route(M, N, K, 4, torch.cuda.get_device_properties(0).multi_processor_count,
+                          w4a8=True) == route
     x = I.make_x_outliers(M, K, 7 + M)
     q = I.make_codes(N, K, 4, 8 + M)
     xq_ref, _ = O.act_quant_ref(x)
-    packed, _ = wq.wna16_repack(to_dev(q), to_dev_bf16(I.make_scales(N, K // 128, 1)), 4)
-    acc = wq.debug_w4a8_group_acc(to_dev(xq_ref), packed, N, K)
-    torch.cuda.synchronize()
+    packed, s_dev = wq.wna16_repack(to_dev(q), to_dev_bf16(I.make_scales(N, K // 128, 1)), 4)
+    g = Guarded((M, N, K // 128), torch.int32)
+    acc = wq.debug_w4a8_group_acc(to_dev_bf16(x), packed, s_dev, N, K, acc=g.t)
+    g.check(f"acc M={M} N={N} K={K}")
     assert np.array_equal(acc.cpu().numpy().astype(np.int64), O.w4a8_group_acc(xq_ref, q))
 
 

@@ -43,7 +43,8 @@ SIGNATURES = {
     "wq_debug_decode_plan": (_c_int, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_ptr]),
     "wq_debug_route": (_c_int, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_ptr]),
     "wq_debug_unpack": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr]),
-    "wq_debug_w4a8_group_acc": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr]),
+    "wq_debug_w4a8_group_acc": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr,
+                                         _c_size, _c_ptr]),
     "wq_debug_noalloc_scratch": (_c_int, [_c_ptr, _c_size, _c_int, _c_ptr]),
     "wq_check_status": (_c_int, []),
     "wq_last_error": (ctypes.c_char_p, []),
@@ -313,11 +314,20 @@ def debug_unpack(packed: torch.Tensor, N: int, K: int, bits: int) -> torch.Tenso
     return codes
 
 
-def debug_w4a8_group_acc(xq: torch.Tensor, packed4: torch.Tensor, N: int, K: int) -> torch.Tensor:
-    M = xq.shape[0]
-    _need(xq, "xq", torch.int8, (M, K))
+def debug_w4a8_group_acc(x: torch.Tensor, packed4: torch.Tensor, scales: torch.Tensor, N: int, K: int,
+                         acc: torch.Tensor | None = None) -> torch.Tensor:
+    """The exact int32 group accumulators [M, N, K/128] of W4A8, from the
+    kernel w4a8_gemm launches for the same shape (x is the bf16 activation,
+    quantized per token exactly as w4a8_gemm does)."""
+    M = x.shape[0]
+    _need(x, "x", torch.bfloat16, (M, K))
     _need(packed4, "packed4", torch.int32, (N, packed_words_per_row(K, 4)))
-    acc = torch.empty((M, N, K // 128), dtype=torch.int32, device=xq.device)
-    _check(load().wq_debug_w4a8_group_acc(_ptr(xq), M, _ptr(packed4), N, K, _ptr(acc), _stream()),
+    _need(scales, "scales", torch.bfloat16, (N, K // 128))
+    if acc is None:
+        acc = torch.empty((M, N, K // 128), dtype=torch.int32, device=x.device)
+    _need(acc, "acc", torch.int32, (M, N, K // 128))
+    scr = scratch(w4a8_scratch_bytes(M, K))
+    _check(load().wq_debug_w4a8_group_acc(_ptr(x), M, _ptr(packed4), _ptr(scales), N, K, _ptr(acc), _ptr(scr),
+                                          scr.numel() * scr.element_size(), _stream()),
            "wq_debug_w4a8_group_acc")
     return acc

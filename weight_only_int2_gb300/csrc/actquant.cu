@@ -17,7 +17,10 @@ namespace {
 constexpr int kThreads = 256;
 
 // kBf16Codes: write each code as a bf16 value (exact, |q| <= 127) instead of
-// int8, for the tensor-core GEMM whose operands are bf16.
+// int8, for the W4A8 tensor-core GEMM whose operands are bf16, and in the K
+// order of its weight operand: within each block of 8 columns the codes of
+// columns 0, 4, 1, 5, 2, 6, 3, 7 (the kernel pairs 4-bit weight codes k and
+// k + 4 of a word; any order shared by both operands gives the same sums).
 template <bool kBf16Codes>
 __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __restrict__ x,
                                                             int64_t K, void* __restrict__ xq_out,
@@ -65,8 +68,8 @@ __global__ void __launch_bounds__(kThreads) act_quant_kernel(const uint16_t* __r
       uint32_t h[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        h[j] = (__float_as_uint(static_cast<float>(q[2 * j])) >> 16) |
-               (__float_as_uint(static_cast<float>(q[2 * j + 1])) & 0xFFFF0000u);
+        h[j] = (__float_as_uint(static_cast<float>(q[j])) >> 16) |
+               (__float_as_uint(static_cast<float>(q[j + 4])) & 0xFFFF0000u);
       reinterpret_cast<uint4*>(static_cast<uint16_t*>(xq_out) + row * K)[i] = make_uint4(h[0], h[1], h[2], h[3]);
     } else {
       uint32_t packed[2] = {0u, 0u};

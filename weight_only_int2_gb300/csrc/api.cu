@@ -173,7 +173,7 @@ wq_status wna16_launch(const Ctx& c, Route r, const uint16_t* x, int64_t M, cons
   a.bits = bits;
   a.y = y;
   a.ws = static_cast<float*>(workspace);
-  cudaError_t e = r == Route::kTensorCore ? launch_prefill(c, x, Wpacked, scales, M, N, K, bits, y, nullptr)
+  cudaError_t e = r == Route::kTensorCore ? launch_prefill(c, x, Wpacked, scales, M, N, K, bits, y)
                                           : launch_routed(c, r, a);
   if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "wna16_gemm launch");
   return WQ_OK;
@@ -345,28 +345,34 @@ size_t w4a8_scratch_bytes(int64_t M, int64_t K) {
   return al256(static_cast<size_t>(M) * K * 2) + al256(static_cast<size_t>(M) * 4);
 }
 
-wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const wq_bf16* scales,
-                    int64_t N, int64_t K, int group, wq_bf16* y, void* workspace, size_t ws_bytes,
-                    void* scratch, size_t scratch_bytes, void* stream) {
-  t_err[0] = 0;
+// W4A8 in full (w4a8_gemm), or its per-group accumulators through the same
+// route and kernel (acc != nullptr: wq_debug_w4a8_group_acc).
+static wq_status w4a8_body(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const wq_bf16* scales,
+                           int64_t N, int64_t K, int group, wq_bf16* y, int32_t* acc, void* workspace,
+                           size_t ws_bytes, void* scratch, size_t scratch_bytes, void* stream) {
   WQ_TRY(check_group_k(group, K, "K"));
   WQ_TRY(check_size(M, "M"));
   WQ_TRY(check_size(N, "N"));
   WQ_PTR(x);
   WQ_PTR(Wpacked4);
   WQ_PTR(scales);
-  WQ_PTR(y);
+  if (acc != nullptr) {
+    WQ_PTR(acc);
+  } else {
+    WQ_PTR(y);
+  }
   WQ_PTR(scratch);
   const size_t need_s = w4a8_scratch_bytes(M, K);
   if (scratch_bytes < need_s)
     return fail(WQ_EINVAL, "scratch too small: %zu < %zu bytes", scratch_bytes, need_s);
   const size_t need = w4a8_workspace_bytes(M, N, K);
-  if (need > 0 && !maybe_tensor_core(M, N, K, 4)) WQ_TRY(check_workspace(workspace, ws_bytes, need));
+  const bool uses_ws = acc == nullptr;  // the group-accumulator mode needs no split-K partials
+  if (uses_ws && need > 0 && !maybe_tensor_core(M, N, K, 4)) WQ_TRY(check_workspace(workspace, ws_bytes, need));
   Ctx c{};
   WQ_TRY(get_ctx(stream, &c));
   const Route r = route_w4a8(M, N, K, c.sm_count);
   if (r == Route::kNone) return no_route(M, N, K);
-  const size_t need_r = route_workspace_bytes(r, M, N, K);
+  const size_t need_r = uses_ws ? route_workspace_bytes(r, M, N, K) : 0;
   if (need_r > 0) {
     WQ_TRY(check_workspace(workspace, ws_bytes, need_r));
     const uintptr_t w0 = reinterpret_cast<uintptr_t>(workspace), s0 = reinterpret_cast<uintptr_t>(scratch);
@@ -376,7 +382,7 @@ wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const
   int8_t* xq = reinterpret_cast<int8_t*>(sb);
   float* sx = reinterpret_cast<float*>(sb + al256(static_cast<size_t>(M) * K * 2));
   GemvArgs a{};
-  a.mode = GemvMode::kW4a8;
+  a.mode = acc != nullptr ? GemvMode::kW4a8GroupAcc : GemvMode::kW4a8;
   a.packed = Wpacked4;
   a.scales = scales;
   a.M = M;
@@ -384,6 +390,7 @@ wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const
   a.K = K;
   a.bits = 4;
   a.y = y;
+  a.acc = acc;
   if (r == Route::kDecodePair) {
     // few tokens: the decode kernel quantizes the activations per token in
     // its staging (same arithmetic as act_quant_int8), no separate pass
@@ -393,12 +400,12 @@ wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const
     return WQ_OK;
   }
   if (r == Route::kTensorCore) {
-    // many tokens: codes as exact bf16 values into the tensor-core GEMM,
-    // which applies sx per output row
+    // many tokens: the codes as exact bf16 values into the tensor-core
+    // kernel, which accumulates each group exactly and applies s and sx
     uint16_t* xqb = reinterpret_cast<uint16_t*>(sb);
     cudaError_t e = launch_act_quant_bf16(c, x, M, K, xqb, sx);
     if (e != cudaSuccess) return cuda_fail(e, "act_quant launch");
-    e = launch_prefill(c, xqb, Wpacked4, scales, M, N, K, 4, y, sx);
+    e = launch_w4a8_tc(c, xqb, sx, Wpacked4, scales, M, N, K, y, acc);
     if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "w4a8_gemm launch");
     return WQ_OK;
   }
@@ -410,6 +417,14 @@ wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const
   e = launch_routed(c, r, a);
   if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "w4a8_gemm launch");
   return WQ_OK;
+}
+
+wq_status w4a8_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const wq_bf16* scales,
+                    int64_t N, int64_t K, int group, wq_bf16* y, void* workspace, size_t ws_bytes,
+                    void* scratch, size_t scratch_bytes, void* stream) {
+  t_err[0] = 0;
+  return w4a8_body(x, M, Wpacked4, scales, N, K, group, y, nullptr, workspace, ws_bytes, scratch, scratch_bytes,
+                   stream);
 }
 
 wq_status qembed_gather(const int32_t* ids, int64_t T, const uint32_t* Wpacked, const wq_bf16* scales,
@@ -473,29 +488,12 @@ wq_status wq_debug_unpack(const uint32_t* packed, int64_t N, int64_t K, int bits
   return WQ_OK;
 }
 
-wq_status wq_debug_w4a8_group_acc(const int8_t* xq, int64_t M, const uint32_t* Wpacked4, int64_t N,
-                                  int64_t K, int32_t* acc, void* stream) {
+wq_status wq_debug_w4a8_group_acc(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4, const wq_bf16* scales,
+                                  int64_t N, int64_t K, int32_t* acc, void* scratch, size_t scratch_bytes,
+                                  void* stream) {
   t_err[0] = 0;
-  WQ_TRY(check_group_k(128, K, "K"));
-  WQ_TRY(check_size(M, "M"));
-  WQ_TRY(check_size(N, "N"));
-  WQ_PTR(xq);
-  WQ_PTR(Wpacked4);
-  WQ_PTR(acc);
-  Ctx c{};
-  WQ_TRY(get_ctx(stream, &c));
-  GemvArgs a{};
-  a.mode = GemvMode::kW4a8GroupAcc;
-  a.xq = xq;
-  a.packed = Wpacked4;
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.bits = 4;
-  a.acc = acc;
-  cudaError_t e = launch_stream_gemm(c, a);
-  if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "group-acc launch");
-  return WQ_OK;
+  if (acc == nullptr) return fail(WQ_EINVAL, "acc is NULL");
+  return w4a8_body(x, M, Wpacked4, scales, N, K, 128, nullptr, acc, nullptr, 0, scratch, scratch_bytes, stream);
 }
 
 wq_status wq_check_status(void) {

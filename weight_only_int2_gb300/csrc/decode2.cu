@@ -59,6 +59,7 @@ struct D2Params {
   int NS;              // ring stages
   int sbox, sx0;       // scale box width, and the box start of each half (x0 of half q = q * sx0)
   uint16_t* y;
+  int32_t* acc;        // kMode 2: int32 [M, N, G] group accumulators
   unsigned* status;
 };
 
@@ -210,10 +211,15 @@ __host__ __device__ inline D2Smem d2_smem(int B, int NT, int T, int H, int Gh, i
   return s;
 }
 
-template <int B, int NT, bool kQuant>
+// kMode 0: WNA16. kMode 1: W4A8 (x quantized per token in the staging).
+// kMode 2: W4A8, and instead of y the exact per-group integer accumulators
+// acc[m, n, g] = sum_{k in g} xq[m, k] (q[n, k] - 8) are written (the test
+// and debug mode of the same main loop; the reduction and exchange still run).
+template <int B, int NT, int kMode>
 __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const __grid_constant__ CUtensorMap smap,
                                                               const D2Params p) {
+  constexpr bool kQuant = kMode >= 1;
   constexpr bool kF16 = uses_fp16<B>();
   constexpr int kTok = NT * 8;  // token columns of the partial-sum buffer
   extern __shared__ uint8_t smem_raw[];
@@ -531,6 +537,26 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
               mma16c<kF16, false>(c[j][1], a2[2], a3[2], a2[3], a3[3], bv.z, bv.w);
             }
           }
+          if constexpr (kMode == 2) {
+            // the group's exact integer sums: xq (128 + q) - 136 xq
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              const int ti0 = (j * 8 + 2 * t) * Gh + gl, ti1 = ti0 + Gh;
+              const float cr0 = corr[ti0], cr1 = corr[ti1], sl0 = scl[ti0], sl1 = scl[ti1];
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int tok = j * 8 + 2 * t + (e & 1);
+                  const int rl = tile * kTileRows + g + 16 * hh + 8 * (e >> 1);
+                  const int64_t row = rc + rl;
+                  if (tok < p.M && rl < H && row < r1) {
+                    const float v = (e & 1) ? fmaf(sl1, c[j][hh][e], -cr1) : fmaf(sl0, c[j][hh][e], -cr0);
+                    p.acc[(static_cast<int64_t>(tok) * p.N + row) * p.G + gbase + gl] = __float2int_rn(v);
+                  }
+                }
+            }
+          }
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
             const int ti0 = (j * 8 + 2 * t) * Gh + gl, ti1 = ti0 + Gh;
@@ -599,7 +625,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           const int rr = e % half_rows, tok = e / half_rows;
           const int rl = static_cast<int>(q) * half_rows + rr;
           const int64_t row = rc + rl;
-          if (tok < p.M && rl < H && row < r1) {  // tile rows past H are not the chunk's
+          if (kMode != 2 && tok < p.M && rl < H && row < r1) {  // tile rows past H are not the chunk's
             float v = part[rl * kTok + tok] + inbox[rr * kTok + tok];
             if constexpr (kQuant) v *= s_sx[tok];
             p.y[tok * p.N + row] = float_to_bf16_bits_rn(v);
@@ -671,10 +697,10 @@ D2Plan make_d2plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
   return pl;
 }
 
-template <int B, int NT, bool kQuant>
+template <int B, int NT, int kMode>
 cudaError_t d2launch(const Ctx& c, const CUtensorMap& wmap, const CUtensorMap& smap, const D2Plan& pl) {
   static SmemLimit limit;  // dynamic smem opted in so far, per device
-  auto kern = decode2_kernel<B, NT, kQuant>;
+  auto kern = decode2_kernel<B, NT, kMode>;
   const cudaError_t e = raise_smem_limit(limit, kern, c.device, pl.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
@@ -696,14 +722,14 @@ cudaError_t d2launch(const Ctx& c, const CUtensorMap& wmap, const CUtensorMap& s
   return cudaLaunchKernelEx(&cfg, kern, wmap, smap, pl.prm);
 }
 
-template <bool kQuant>
+template <int kMode>
 cudaError_t d2launch_b(const Ctx& c, int bits, const CUtensorMap& wmap, const CUtensorMap& smap, const D2Plan& pl) {
-  if constexpr (kQuant) {
+  if constexpr (kMode >= 1) {
     if (bits != 4) return cudaErrorInvalidValue;
-    return pl.NT == 1 ? d2launch<4, 1, true>(c, wmap, smap, pl) : d2launch<4, 2, true>(c, wmap, smap, pl);
+    return pl.NT == 1 ? d2launch<4, 1, kMode>(c, wmap, smap, pl) : d2launch<4, 2, kMode>(c, wmap, smap, pl);
   } else {
 #define WQ_D2(BB) \
-  case BB: return pl.NT == 1 ? d2launch<BB, 1, false>(c, wmap, smap, pl) : d2launch<BB, 2, false>(c, wmap, smap, pl);
+  case BB: return pl.NT == 1 ? d2launch<BB, 1, 0>(c, wmap, smap, pl) : d2launch<BB, 2, 0>(c, wmap, smap, pl);
     switch (bits) {
       WQ_D2(2)
       WQ_D2(3)
@@ -750,14 +776,16 @@ int decode2_plan_info(int64_t M, int64_t N, int64_t K, int bits, int sm_count, i
 }
 
 cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a) {
-  // kW4a8 here: a.x is the bf16 activation, quantized per token in the kernel
-  const bool quant = a.mode == GemvMode::kW4a8;
-  if (a.mode != GemvMode::kWna16 && !quant) return cudaErrorInvalidValue;
+  // the W4A8 modes here take a.x, the bf16 activations, and quantize them per
+  // token in the kernel; kW4a8GroupAcc writes a.acc instead of a.y
+  const int mode = a.mode == GemvMode::kWna16 ? 0 : a.mode == GemvMode::kW4a8 ? 1 : 2;
+  if (a.x == nullptr || (mode == 2 && a.acc == nullptr)) return cudaErrorInvalidValue;
   const D2Plan pl = make_d2plan(a.M, a.N, a.K, a.bits, c.sm_count);
   if (!pl.ok) return cudaErrorInvalidValue;
   D2Plan q = pl;
   q.prm.x = a.x;
   q.prm.y = a.y;
+  q.prm.acc = a.acc;
   q.prm.status = c.status;
   CUtensorMap wmap, smap;
   const uint64_t words = static_cast<uint64_t>(a.K) * a.bits / 32;
@@ -767,7 +795,9 @@ cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a) {
   if (!make_tmap_bf16_2d(&smap, a.scales, static_cast<uint64_t>(pl.prm.G), static_cast<uint64_t>(a.N),
                          static_cast<uint32_t>(pl.prm.sbox), static_cast<uint32_t>(pl.prm.H)))
     return cudaErrorInvalidValue;
-  return quant ? d2launch_b<true>(c, a.bits, wmap, smap, q) : d2launch_b<false>(c, a.bits, wmap, smap, q);
+  if (mode == 1) return d2launch_b<1>(c, a.bits, wmap, smap, q);
+  if (mode == 2) return d2launch_b<2>(c, a.bits, wmap, smap, q);
+  return d2launch_b<0>(c, a.bits, wmap, smap, q);
 }
 
 }  // namespace wq

@@ -95,6 +95,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// mbar_wait_bounded for a waiter with slack (a producer rings ahead, or a
+// consumer a whole stage ahead of its deadline): after each failed poll the
+// warp sleeps about kSleepNs, so that its polling does not take issue slots
+// from the warps doing the work. Same bound and result as mbar_wait_bounded.
+template <uint32_t kSleepNs>
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i) {
+      __nanosleep(kSleepNs);
+      if (mbar_try_wait(bar, parity)) return true;
+    }
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // atom.add with acquire-release semantics at GPU scope; returns the old value.
 __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* addr, unsigned v) {
   unsigned old;

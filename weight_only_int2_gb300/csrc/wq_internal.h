@@ -69,8 +69,9 @@ cudaError_t launch_unpack(const Ctx& c, const uint32_t* packed, int64_t N, int64
 cudaError_t launch_act_quant(const Ctx& c, const uint16_t* x, int64_t M, int64_t K, int8_t* xq,
                              float* sx);
 
-// Same quantization, codes written as bf16 values (exact) for the
-// tensor-core GEMM.
+// Same quantization, codes written as bf16 values (exact) for the W4A8
+// tensor-core GEMM, in its K order: within each block of 8 columns the codes
+// of columns 0, 4, 1, 5, 2, 6, 3, 7.
 cudaError_t launch_act_quant_bf16(const Ctx& c, const uint16_t* x, int64_t M, int64_t K, uint16_t* xqb,
                                   float* sx);
 
@@ -110,11 +111,17 @@ size_t decode_workspace_bytes(int64_t M, int64_t N);
 cudaError_t launch_decode(const Ctx& c, const GemvArgs& a);
 
 // Tensor-core GEMM for many tokens (tcgen05, dequantize-then-multiply).
-// sx, when given, multiplies output row m (the W4A8 per-token factor).
 constexpr int64_t kPrefillMinTokens = 65;
 bool prefill_supported(int64_t M, int64_t N, int64_t K, int bits);
 cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* packed, const uint16_t* scales,
-                           int64_t M, int64_t N, int64_t K, int bits, uint16_t* y, const float* sx);
+                           int64_t M, int64_t N, int64_t K, int bits, uint16_t* y);
+
+// W4A8 on the tensor cores with exact per-group integer accumulation
+// (w4a8tc.cu): xqb holds the per-token int8 codes as bf16 values [M, K] and sx
+// the token scales [M]; writes y [M, N], or with acc != nullptr the group
+// accumulators acc [M, N, K/128] (int32) instead.
+cudaError_t launch_w4a8_tc(const Ctx& c, const uint16_t* xqb, const float* sx, const uint32_t* packed4,
+                           const uint16_t* scales, int64_t M, int64_t N, int64_t K, uint16_t* y, int32_t* acc);
 
 // From kPrefillMinTokens tokens on, always; from 32 tokens when the layer has
 // at least one 128-row tile per two SMs. Measured at K = 5120 (b = 5..7): the
@@ -141,15 +148,6 @@ int decode2_plan_info(int64_t M, int64_t N, int64_t K, int bits, int sm_count, i
 bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count);
 cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a);
 
-// Routes a weight-streaming GEMM (few tokens): WNA16 to the CTA-pair decode
-// kernel when it applies; otherwise (and W4A8 with precomputed int8 codes) the
-// persistent split-K decode kernel, else the chunked kernel.
-inline cudaError_t launch_stream_gemm(const Ctx& c, const GemvArgs& a) {
-  if (a.mode == GemvMode::kWna16 && decode2_supported(a.M, a.N, a.K, a.bits, c.sm_count))
-    return launch_decode2(c, a);
-  return decode_supported(a.M, a.N, a.K, a.bits, c.sm_count) ? launch_decode(c, a) : launch_gemv(c, a);
-}
-
 // The kernel a GEMM call launches, by shape (host only). The entry points
 // dispatch on it and wq_debug_route reports it; the values are the header's
 // WQ_ROUTE_* numbers.
@@ -168,8 +166,9 @@ inline Route route_wna16(int64_t M, int64_t N, int64_t K, int bits, int sm_count
 }
 
 // W4A8: the pair kernel quantizes few tokens itself; for many tokens the codes
-// go as exact bf16 values into the tensor-core kernel; otherwise int8 codes
-// feed the split-K streaming kernels.
+// go as exact bf16 values into the W4A8 tensor-core kernel (w4a8tc.cu, exact
+// per-group accumulation); otherwise int8 codes feed the split-K streaming
+// kernels.
 inline Route route_w4a8(int64_t M, int64_t N, int64_t K, int sm_count) {
   if (decode2_supported(M, N, K, 4, sm_count)) return Route::kDecodePair;
   if (use_prefill(M, N, K, 4, sm_count)) return Route::kTensorCore;
