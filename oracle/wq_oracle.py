@@ -170,6 +170,42 @@ def wna16_ref(x_bits, codes, scales_bits, bits: int, group: int = GROUP) -> np.n
 
 
 # --------------------------------------------------------------------------
+# Asymmetric groups: a zero point per (output row, group)
+# --------------------------------------------------------------------------
+# Model card "Qwen3.8-27B-INT6-Mixed-AutoRound", section "Findings", second
+# bullet: asymmetric quantization (a zero point per group, not the symmetric
+# 2^(b-1)) is what the four-bit tier of the previous build used, worth about a
+# quarter of a bit; the serving path there offered it only at 4 and 8 bits.
+# The page prints no layout. Readings adopted here: one integer zero point per
+# (output row, 128-wide group), stored one byte each [N, K // group], of which
+# the low ``bits`` bits are used (as for codes), and w = s * (q - zp).
+
+def zero_points_used(zeros, bits: int) -> np.ndarray:
+    """The zero points the layer uses: the low ``bits`` bits of each byte."""
+    return np.asarray(zeros).astype(np.int64) & ((1 << int(bits)) - 1)
+
+
+def dequant_zp(codes, scales_bits, zeros, bits: int, group: int = GROUP) -> np.ndarray:
+    """w[n, k] = s[n, k // group] * (q[n, k] - zp[n, k // group]) in float64
+    (every product exact)."""
+    q = np.asarray(codes).astype(np.float64)
+    N, K = q.shape
+    if K % group:
+        raise ValueError("K must be a multiple of the group size")
+    s = bf16_bits_to_f64(scales_bits)
+    zp = zero_points_used(zeros, bits).astype(np.float64)
+    if s.shape != (N, K // group) or zp.shape != (N, K // group):
+        raise ValueError("scales and zeros must be [N, K // group]")
+    return np.repeat(s, group, axis=1) * (q - np.repeat(zp, group, axis=1))
+
+
+def wna16_zp_ref(x_bits, codes, scales_bits, zeros, bits: int, group: int = GROUP) -> np.ndarray:
+    """y = x . dequant_zp(W)^T in float64."""
+    x = bf16_bits_to_f64(x_bits)
+    return x @ dequant_zp(codes, scales_bits, zeros, bits, group).T
+
+
+# --------------------------------------------------------------------------
 # W4A8: per-token int8 activation quantization and integer accumulation
 # --------------------------------------------------------------------------
 

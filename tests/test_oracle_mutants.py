@@ -49,6 +49,12 @@ def _pin_calls():
     for b in (5, 6):
         for kind in ("zero_point", "min", "max"):
             calls.append((f"closed form b{b} {kind}", P.test_wna16_closed_form_constant_codes, (b, kind)))
+    for b in (5, 8):
+        calls.append((f"zp brute force b{b}", P.test_zp_brute_force_exact_rationals, (b,)))
+        calls.append((f"zp closed form b{b}", P.test_zp_closed_form_constant_codes, (b,)))
+        calls.append((f"zp at half range b{b}", P.test_zp_at_half_range_is_the_symmetric_layer, (b,)))
+    calls.append(("zp shift invariance", P.test_zp_shift_invariance, ()))
+    calls.append(("zp low bits", P.test_zp_uses_the_low_bits_of_each_byte, ()))
     return calls
 
 
@@ -281,7 +287,35 @@ def _bytes_scale_per_row(rows, cols, bits, group=W.GROUP):
     return int(rows) * (W.packed_words_per_row(cols, bits) * 4 + 2)
 
 
+def _dequant_zp_variant(kind):
+    def f(codes, scales_bits, zeros, bits, group=W.GROUP):
+        q = np.asarray(codes).astype(np.float64)
+        N, K = q.shape
+        s = np.repeat(W.bf16_bits_to_f64(scales_bits), group, axis=1)
+        zp = W.zero_points_used(zeros, bits).astype(np.float64)
+        if kind == "ignored":          # the symmetric zero point instead
+            return s * (q - float(W.zero_point(bits)))
+        if kind == "added":            # sign of the zero point flipped
+            return s * (q + np.repeat(zp, group, axis=1))
+        if kind == "tiled":            # group index k mod G instead of k // group
+            G = K // group
+            return s * (q - zp[:, np.arange(K) % G])
+        if kind == "unmasked":         # every bit of the byte used
+            return s * (q - np.repeat(np.asarray(zeros).astype(np.float64), group, axis=1))
+        raise ValueError(kind)
+    return f
+
+
+def _zp_bits_masked_wrong(zeros, bits):
+    return np.asarray(zeros).astype(np.int64) & ((1 << (int(bits) - 1)) - 1)
+
+
 MUTANTS = {
+    "zero point per group ignored": {"dequant_zp": _dequant_zp_variant("ignored")},
+    "zero point added instead of subtracted": {"dequant_zp": _dequant_zp_variant("added")},
+    "zero point indexed k mod G": {"dequant_zp": _dequant_zp_variant("tiled")},
+    "zero point high bits used": {"dequant_zp": _dequant_zp_variant("unmasked")},
+    "zero point masked to bits - 1": {"zero_points_used": _zp_bits_masked_wrong},
     "stream bits MSB-first in each word (pack and unpack)": {"pack": _pack_msb, "unpack": _unpack_msb},
     "each code's bits reversed (pack and unpack)": {"pack": _pack_codes_msb_first,
                                                    "unpack": _unpack_codes_msb_first},

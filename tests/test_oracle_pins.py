@@ -438,3 +438,85 @@ def test_stack_allocation():
     bits = [I.stack_layer_bits(l) for l in range(64)]
     assert bits[:10] == [7] * 10 and bits[54:] == [7] * 10
     assert bits[10:54] == [5, 6] * 22
+
+
+# ---------------------------------------------------------------- asymmetric groups
+
+def _zeros(N, G, bits, seed):
+    return np.random.default_rng(seed).integers(0, 1 << bits, size=(N, G)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 7, 8])
+def test_zp_brute_force_exact_rationals(bits):
+    """w = s (q - zp[n, g]) against exact rational arithmetic on a tiny
+    shape with a different zero point in every (row, group)."""
+    M, K, N = 2, 256, 3
+    x = I.make_x(M, K, 41 + bits)
+    q = I.make_codes(N, K, bits, 42 + bits)
+    s = I.make_scales(N, K // 128, 43 + bits)
+    zp = _zeros(N, K // 128, bits, 44 + bits)
+    y = O.wna16_zp_ref(x, q, s, zp, bits)
+    for m in range(M):
+        for n in range(N):
+            exact = Fraction(0)
+            mag = Fraction(0)
+            for k in range(K):
+                term = _frac_bf16(x[m, k]) * _frac_bf16(s[n, k // 128]) * (int(q[n, k]) - int(zp[n, k // 128]))
+                exact += term
+                mag += abs(term)
+            assert abs(Fraction(float(y[m, n])) - exact) <= mag * Fraction(1, 2**45)
+
+
+@pytest.mark.parametrize("bits", [5, 6, 8])
+def test_zp_closed_form_constant_codes(bits):
+    """All codes c: y[m, n] = sum_g s[n, g] (c - zp[n, g]) sum_{k in g} x[m, k];
+    codes equal to each group's zero point give y == 0 exactly."""
+    M, K, N = 2, 384, 5
+    G = K // 128
+    x = I.make_x(M, K, 51)
+    s = I.make_scales(N, G, 52)
+    zp = _zeros(N, G, bits, 53)
+    c = (1 << bits) - 1
+    q = np.full((N, K), c, dtype=np.int64)
+    y = O.wna16_zp_ref(x, q, s, zp, bits)
+    xg = O.bf16_bits_to_f64(x).reshape(M, G, 128).sum(axis=2)              # [M, G]
+    coef = O.bf16_bits_to_f64(s) * (c - zp.astype(np.float64))             # [N, G]
+    np.testing.assert_allclose(y, xg @ coef.T, rtol=1e-12, atol=1e-12)
+    qz = np.repeat(zp.astype(np.int64), 128, axis=1)
+    assert np.all(O.wna16_zp_ref(x, qz, s, zp, bits) == 0.0)
+
+
+@pytest.mark.parametrize("bits", [5, 6, 7, 8])
+def test_zp_at_half_range_is_the_symmetric_layer(bits):
+    M, K, N = 3, 256, 6
+    x = I.make_x(M, K, 61)
+    q = I.make_codes(N, K, bits, 62)
+    s = I.make_scales(N, K // 128, 63)
+    zp = np.full((N, K // 128), 1 << (bits - 1), dtype=np.uint8)
+    assert np.array_equal(O.wna16_zp_ref(x, q, s, zp, bits), O.wna16_ref(x, q, s, bits))
+
+
+def test_zp_shift_invariance():
+    """Shifting the codes and the zero point of a group by the same amount
+    leaves the dequantized weights, hence y, unchanged."""
+    bits, M, K, N = 6, 2, 256, 4
+    x = I.make_x(M, K, 71)
+    s = I.make_scales(N, K // 128, 72)
+    rng = np.random.default_rng(73)
+    q = rng.integers(0, 40, size=(N, K))
+    zp = rng.integers(0, 40, size=(N, K // 128)).astype(np.uint8)
+    d = np.array([[3, 17], [0, 23], [11, 5], [20, 1]])                    # per (row, group)
+    q2 = q + np.repeat(d, 128, axis=1)
+    zp2 = (zp.astype(np.int64) + d).astype(np.uint8)
+    assert np.array_equal(O.wna16_zp_ref(x, q, s, zp, bits), O.wna16_zp_ref(x, q2, s, zp2, bits))
+
+
+def test_zp_uses_the_low_bits_of_each_byte():
+    bits, M, K, N = 5, 2, 256, 3
+    x = I.make_x(M, K, 81)
+    q = I.make_codes(N, K, bits, 82)
+    s = I.make_scales(N, K // 128, 83)
+    zp = _zeros(N, K // 128, bits, 84)
+    high = (zp | np.uint8(0xE0)).astype(np.uint8)                          # bits 5..7 set
+    assert np.array_equal(O.wna16_zp_ref(x, q, s, high, bits), O.wna16_zp_ref(x, q, s, zp, bits))
+    assert O.zero_points_used(np.array([0xFF], dtype=np.uint8), 5)[0] == 31
