@@ -115,6 +115,25 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
                      int64_t N, int64_t K, int bits, int group, wq_bf16* y,
                      void* workspace, size_t ws_bytes, void* stream);
 
+/* WNA16 linear layer with asymmetric groups [CARD "Findings", second bullet:
+ * a zero point per group instead of the symmetric 2^(bits-1), the option the
+ * pages' four-bit tier used and their serving path lacked above four bits]:
+ *   y[m, n] = sum_k x[m, k] * s[n, k/128] * (q[n, k] - zp[n, k/128]),
+ * float32 accumulation, y rounded to bf16.
+ *  zeros    [N, K/128] uint8, one zero point per (row, group); its low `bits`
+ *           bits are used (the method's zero points lie in [0, 2^bits - 1]).
+ *  Every other argument as wna16_gemm; workspace at least
+ *  wna16_zp_workspace_bytes(). Same kernels as wna16_gemm, except that
+ *  few-token shapes whose K half does not fit the CTA-pair decode kernel go
+ *  to the chunked kernel (K <= 16384; larger K returns WQ_EUNSUPPORTED). */
+wq_status wna16_gemm_zp(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const wq_bf16* scales,
+                        const uint8_t* zeros, int64_t N, int64_t K, int bits, int group, wq_bf16* y,
+                        void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes wna16_gemm_zp needs (same contract as
+ * wna16_workspace_bytes). */
+size_t wna16_zp_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits);
+
 /* WNA16 linear layer without a workspace argument, for callers that cannot
  * allocate device memory (no counterpart on the source pages; it is a
  * packaging of wna16_gemm). A serving engine that has reserved nearly all
@@ -202,18 +221,19 @@ wq_status qembed_gather(const int32_t* ids, int64_t T, const uint32_t* Wpacked,
  * outside 2..8, sm_count < 1 or a NULL out14. */
 wq_status wq_debug_decode_plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count, int64_t* out14);
 
-/* Which kernel wna16_gemm (w4a8 = 0) or w4a8_gemm (w4a8 = 1, bits = 4) launches
- * for a shape on a device with sm_count SMs (host only, no device call). The
- * entry points dispatch on the same function. *route receives one of: */
+/* Which kernel wna16_gemm (kind = 0), w4a8_gemm (kind = 1, bits = 4) or
+ * wna16_gemm_zp (kind = 2) launches for a shape on a device with sm_count SMs
+ * (host only, no device call). The entry points dispatch on the same
+ * function. *route receives one of: */
 #define WQ_ROUTE_NONE 0          /* no kernel takes the shape: the call returns WQ_EUNSUPPORTED */
 #define WQ_ROUTE_DECODE_PAIR 1   /* CTA-pair decode kernel: M <= 16, K % 1024 == 0 */
 #define WQ_ROUTE_DECODE_SPLITK 2 /* persistent split-K decode kernel (uses the workspace) */
 #define WQ_ROUTE_CHUNKED 3       /* chunked split-K streaming kernel (uses the workspace) */
 #define WQ_ROUTE_TENSOR_CORE 4   /* tcgen05 tensor-core GEMM: M >= 65, or 32..64 tokens on a
                                     layer with a 128-row tile for every two SMs */
-/* WQ_EINVAL for a NULL route, sm_count < 1, w4a8 not 0/1, bits outside 2..8
- * (not 4 with w4a8), K not a positive multiple of 128, or M, N < 1. */
-wq_status wq_debug_route(int64_t M, int64_t N, int64_t K, int bits, int w4a8, int sm_count, int* route);
+/* WQ_EINVAL for a NULL route, sm_count < 1, kind not 0..2, bits outside 2..8
+ * (not 4 with kind 1), K not a positive multiple of 128, or M, N < 1. */
+wq_status wq_debug_route(int64_t M, int64_t N, int64_t K, int bits, int kind, int sm_count, int* route);
 
 /* Inverse of the repack for the codes: packed [N, ceil(K*bits/32)] ->
  * codes [N, K] uint8. */
@@ -230,6 +250,17 @@ wq_status wq_debug_unpack(const uint32_t* packed, int64_t N, int64_t K, int bits
 wq_status wq_debug_w4a8_group_acc(const wq_bf16* x, int64_t M, const uint32_t* Wpacked4,
                                   const wq_bf16* scales, int64_t N, int64_t K, int32_t* acc,
                                   void* scratch, size_t scratch_bytes, void* stream);
+
+/* Test hook of the CTA-pair decode kernel, for checking the bounded-wait error
+ * path without any fault: from the next launch on the current device, every
+ * pipeline wait of that kernel gives up after wait_limit_ns (0: the default
+ * bound of 2 s), and its producers stop issuing weight stages at stage
+ * stop_stage of their sequence (-1: never). The copies already issued all
+ * land; the consumers waiting for the first stage never issued give up,
+ * record WQ_ETIMEOUT (read by wq_check_status) and finish the kernel, whose
+ * outputs are then incomplete. Call again with (-1, 0) to restore normal
+ * operation. Synchronous. */
+wq_status wq_debug_decode_wait_fault(int64_t stop_stage, uint64_t wait_limit_ns);
 
 /* Copies `bytes` (at most 4 MiB) between the caller's device buffer `buf` and
  * the start of wna16_gemm_noalloc's scratch array on the current device

@@ -121,3 +121,36 @@ def test_zero_query_means_the_pair_kernel_on_every_device():
                     routes = {wq.debug_route(M, N, K, bits, sms) for sms in sms_list}
                     if zero:
                         assert routes == {"decode_pair"}, (M, N, K, bits, routes)
+
+
+def test_zero_point_routes_and_workspace_query():
+    """Asymmetric groups: the same kernels except the persistent split-K
+    decode kernel (no zero-point mode), whose shapes the chunked kernel takes;
+    the zero-point workspace query covers the need of every route it can
+    take, across shapes and SM counts."""
+    import random
+
+    from weight_only_int2_gb300 import _lib as L
+
+    lib = L.load()
+    rnd = random.Random(7)
+    seen = set()
+    for _ in range(4000):
+        M = rnd.choice([1, 2, 4, 8, 9, 16, 17, 31, 32, 48, 64, 65, 300])
+        N = rnd.choice([1, 37, 300, 5120, 17408, 60000])
+        K = 128 * rnd.choice([1, 5, 8, 16, 40, 56, 64, 112, 128, 136])
+        bits = rnd.randint(2, 8)
+        sms = rnd.choice([2, 20, 132, 148, 152])
+        r = wq.debug_route(M, N, K, bits, sms, zp=True)
+        seen.add(r)
+        assert r != "decode_splitk"
+        need = wq.wna16_zp_workspace_bytes(M, N, K, bits)
+        if r == "chunked":
+            assert need >= M * N * 4, (M, N, K, bits, sms)
+        if r == "none":
+            assert K > 16384
+        sym = wq.debug_route(M, N, K, bits, sms)
+        if sym == "tensor_core":
+            assert r == "tensor_core"
+    assert {"decode_pair", "chunked", "tensor_core"} <= seen
+    assert lib.wna16_zp_workspace_bytes(1, 17408, 5120, 6) == 0

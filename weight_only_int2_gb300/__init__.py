@@ -25,7 +25,9 @@ from ._lib import (  # noqa: F401
     scratch,
     wna16_gemm,
     wna16_gemm_noalloc,
+    wna16_gemm_zp,
     wna16_repack,
     wna16_workspace_bytes,
+    wna16_zp_workspace_bytes,
     workspace,
 )

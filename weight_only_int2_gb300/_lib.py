@@ -31,6 +31,9 @@ SIGNATURES = {
     "wna16_workspace_bytes": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int]),
     "wna16_gemm": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_int, _c_int, _c_ptr,
                             _c_ptr, _c_size, _c_ptr]),
+    "wna16_gemm_zp": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_int, _c_int, _c_ptr,
+                               _c_ptr, _c_size, _c_ptr]),
+    "wna16_zp_workspace_bytes": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int]),
     "wna16_gemm_noalloc": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_int, _c_int,
                                     _c_ptr, _c_ptr]),
     "act_quant_int8": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr, _c_ptr]),
@@ -46,6 +49,7 @@ SIGNATURES = {
     "wq_debug_w4a8_group_acc": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr,
                                          _c_size, _c_ptr]),
     "wq_debug_noalloc_scratch": (_c_int, [_c_ptr, _c_size, _c_int, _c_ptr]),
+    "wq_debug_decode_wait_fault": (_c_int, [_c_i64, ctypes.c_uint64]),
     "wq_check_status": (_c_int, []),
     "wq_last_error": (ctypes.c_char_p, []),
     "wq_version": (ctypes.c_char_p, []),
@@ -160,6 +164,10 @@ def wna16_workspace_bytes(M: int, N: int, K: int, bits: int) -> int:
     return int(load().wna16_workspace_bytes(M, N, K, bits))
 
 
+def wna16_zp_workspace_bytes(M: int, N: int, K: int, bits: int) -> int:
+    return int(load().wna16_zp_workspace_bytes(M, N, K, bits))
+
+
 def w4a8_workspace_bytes(M: int, N: int, K: int) -> int:
     return int(load().w4a8_workspace_bytes(M, N, K))
 
@@ -215,6 +223,28 @@ def wna16_gemm(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, N: i
     _check(load().wna16_gemm(_ptr(x), M, _ptr(packed), _ptr(scales), N, K, bits, group, _ptr(y),
                              _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _stream()),
            "wna16_gemm")
+    return y
+
+
+def wna16_gemm_zp(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, zeros: torch.Tensor, N: int,
+                  K: int, bits: int, group: int = 128, y: torch.Tensor | None = None,
+                  ws: torch.Tensor | None = None):
+    """y[M, N] = x[M, K] . dequant(W)^T with a zero point per (row, group):
+    w = s * (q - zp); zeros uint8 [N, K/128]."""
+    M = x.shape[0]
+    _need(x, "x", torch.bfloat16, (M, K))
+    _need(packed, "packed", torch.int32, (N, packed_words_per_row(K, bits)))
+    _need(scales, "scales", torch.bfloat16, (N, K // group))
+    _need(zeros, "zeros", torch.uint8, (N, K // group))
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", torch.bfloat16, (M, N))
+    need = wna16_zp_workspace_bytes(M, N, K, bits)
+    if ws is None:
+        ws = workspace(need)
+    _check(load().wna16_gemm_zp(_ptr(x), M, _ptr(packed), _ptr(scales), _ptr(zeros), N, K, bits, group, _ptr(y),
+                                _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _stream()),
+           "wna16_gemm_zp")
     return y
 
 
@@ -299,11 +329,13 @@ def debug_decode_plan(M: int, N: int, K: int, bits: int, sm_count: int) -> dict:
 ROUTES = {0: "none", 1: "decode_pair", 2: "decode_splitk", 3: "chunked", 4: "tensor_core"}
 
 
-def debug_route(M: int, N: int, K: int, bits: int, sm_count: int, w4a8: bool = False) -> str:
-    """Which kernel wna16_gemm (or w4a8_gemm) launches for a shape on a device
-    with sm_count SMs (host only): one of the ROUTES names."""
+def debug_route(M: int, N: int, K: int, bits: int, sm_count: int, w4a8: bool = False, zp: bool = False) -> str:
+    """Which kernel wna16_gemm (or w4a8_gemm, or with zp wna16_gemm_zp)
+    launches for a shape on a device with sm_count SMs (host only): one of the
+    ROUTES names."""
     out = ctypes.c_int(0)
-    _check(load().wq_debug_route(M, N, K, bits, int(bool(w4a8)), sm_count, ctypes.byref(out)), "wq_debug_route")
+    kind = 1 if w4a8 else (2 if zp else 0)
+    _check(load().wq_debug_route(M, N, K, bits, kind, sm_count, ctypes.byref(out)), "wq_debug_route")
     return ROUTES[out.value]
 
 

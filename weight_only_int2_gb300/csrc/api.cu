@@ -153,27 +153,29 @@ bool maybe_tensor_core(int64_t M, int64_t N, int64_t K, int bits) {
   return M >= 32 && M < kPrefillMinTokens && prefill_supported(M, N, K, bits);
 }
 
-wq_status wna16_route(int64_t M, int64_t N, int64_t K, int bits, void* stream, Ctx* c, Route* r) {
+wq_status wna16_route(int64_t M, int64_t N, int64_t K, int bits, void* stream, Ctx* c, Route* r, bool zp) {
   WQ_TRY(get_ctx(stream, c));
-  *r = route_wna16(M, N, K, bits, c->sm_count);
+  *r = zp ? route_wna16_zp(M, N, K, bits, c->sm_count) : route_wna16(M, N, K, bits, c->sm_count);
   if (*r == Route::kNone) return no_route(M, N, K);
   return WQ_OK;
 }
 
 wq_status wna16_launch(const Ctx& c, Route r, const uint16_t* x, int64_t M, const uint32_t* Wpacked,
-                       const uint16_t* scales, int64_t N, int64_t K, int bits, uint16_t* y, void* workspace) {
+                       const uint16_t* scales, int64_t N, int64_t K, int bits, uint16_t* y, void* workspace,
+                       const uint8_t* zeros) {
   GemvArgs a{};
   a.mode = GemvMode::kWna16;
   a.x = x;
   a.packed = Wpacked;
   a.scales = scales;
+  a.zeros = zeros;
   a.M = M;
   a.N = N;
   a.K = K;
   a.bits = bits;
   a.y = y;
   a.ws = static_cast<float*>(workspace);
-  cudaError_t e = r == Route::kTensorCore ? launch_prefill(c, x, Wpacked, scales, M, N, K, bits, y)
+  cudaError_t e = r == Route::kTensorCore ? launch_prefill(c, x, Wpacked, scales, M, N, K, bits, y, zeros)
                                           : launch_routed(c, r, a);
   if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "wna16_gemm launch");
   return WQ_OK;
@@ -315,6 +317,27 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
   const size_t need_r = route_workspace_bytes(r, M, N, K);
   if (need_r > 0) WQ_TRY(check_workspace(workspace, ws_bytes, need_r));
   return wna16_launch(c, r, x, M, Wpacked, scales, N, K, bits, y, workspace);
+}
+
+size_t wna16_zp_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits) {
+  if (M < 1 || N < 1 || K < 128) return 0;
+  return stream_workspace_bytes_zp(M, N, K, bits);
+}
+
+wq_status wna16_gemm_zp(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const wq_bf16* scales,
+                        const uint8_t* zeros, int64_t N, int64_t K, int bits, int group, wq_bf16* y,
+                        void* workspace, size_t ws_bytes, void* stream) {
+  t_err[0] = 0;
+  WQ_TRY(wna16_check_args(x, M, Wpacked, scales, N, K, bits, group, y));
+  WQ_PTR(zeros);
+  const size_t need = stream_workspace_bytes_zp(M, N, K, bits);
+  if (need > 0 && !maybe_tensor_core(M, N, K, bits)) WQ_TRY(check_workspace(workspace, ws_bytes, need));
+  Ctx c{};
+  Route r = Route::kNone;
+  WQ_TRY(wna16_route(M, N, K, bits, stream, &c, &r, true));
+  const size_t need_r = route_workspace_bytes(r, M, N, K);
+  if (need_r > 0) WQ_TRY(check_workspace(workspace, ws_bytes, need_r));
+  return wna16_launch(c, r, x, M, Wpacked, scales, N, K, bits, y, workspace, zeros);
 }
 
 wq_status act_quant_int8(const wq_bf16* x, int64_t M, int64_t K, int8_t* xq, float* sx,
@@ -459,8 +482,8 @@ wq_status wq_debug_route(int64_t M, int64_t N, int64_t K, int bits, int w4a8, in
   t_err[0] = 0;
   if (route == nullptr) return fail(WQ_EINVAL, "route is NULL");
   if (sm_count < 1) return fail(WQ_EINVAL, "sm_count must be >= 1");
-  if (w4a8 != 0 && w4a8 != 1) return fail(WQ_EINVAL, "w4a8 must be 0 or 1");
-  if (w4a8) {
+  if (w4a8 < 0 || w4a8 > 2) return fail(WQ_EINVAL, "kind must be 0, 1 or 2");
+  if (w4a8 == 1) {
     if (bits != 4) return fail(WQ_EINVAL, "W4A8 weights are 4-bit (got bits = %d)", bits);
   } else {
     WQ_TRY(check_bits(bits));
@@ -468,7 +491,9 @@ wq_status wq_debug_route(int64_t M, int64_t N, int64_t K, int bits, int w4a8, in
   WQ_TRY(check_group_k(128, K, "K"));
   WQ_TRY(check_size(M, "M"));
   WQ_TRY(check_size(N, "N"));
-  const Route r = w4a8 ? route_w4a8(M, N, K, sm_count) : route_wna16(M, N, K, bits, sm_count);
+  const Route r = w4a8 == 1   ? route_w4a8(M, N, K, sm_count)
+                  : w4a8 == 2 ? route_wna16_zp(M, N, K, bits, sm_count)
+                              : route_wna16(M, N, K, bits, sm_count);
   *route = static_cast<int>(r);
   return WQ_OK;
 }

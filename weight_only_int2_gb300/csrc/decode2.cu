@@ -60,8 +60,18 @@ struct D2Params {
   int sbox, sx0;       // scale box width, and the box start of each half (x0 of half q = q * sx0)
   uint16_t* y;
   int32_t* acc;        // kMode 2: int32 [M, N, G] group accumulators
+  const uint8_t* zeros;  // kMode 3: zero points [N, G]
   unsigned* status;
 };
+
+// The bound of every wait of this kernel, and a test hook: a producer stops
+// issuing at this stage of its sequence (-1: never). Set through
+// wq_debug_decode_wait_fault, so that a test can make a wait run out: the
+// copies already issued all land, and the consumers that wait for the first
+// stage never issued give up after the bound, record WQ_ETIMEOUT and finish
+// the kernel normally.
+__constant__ uint64_t c_wait_limit_ns = kWaitLimitNs;
+__constant__ int64_t c_stop_stage = -1;
 
 // ---- cluster helpers (inline PTX) -------------------------------------------
 
@@ -103,14 +113,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 // Bounded wait on a barrier that the peer CTA arrives on (cluster scope).
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 __device__ __forceinline__ void st_peer_v4(uint32_t cluster_addr, float4 v) {
@@ -140,14 +150,6 @@ __device__ __forceinline__ void raw_to_float(const uint4 (&r)[4], float (&v)[32]
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory");
 }
-// Named barrier 2 (all threads): the producer warp arrives once the
-// mbarriers are initialised, without waiting; the consumers wait on it
-// before their first mbarrier operation.
-__device__ __forceinline__ void init_done_arrive() {
-  asm volatile("bar.arrive 2, %0;" ::"n"(kThreads2) : "memory");
-}
-__device__ __forceinline__ void init_done_wait() { asm volatile("bar.sync 2, %0;" ::"n"(kThreads2) : "memory"); }
-
 // m16n8k16 MMA with f32 accumulators, D = A B + C (kZero: C = 0). Not
 // volatile: the compiler may schedule it like any other arithmetic.
 template <bool kF16, bool kZero>
@@ -192,9 +194,10 @@ __device__ __forceinline__ void unpack_quad2(const uint32_t (&w)[B], int i2, uin
 // next region, whose results are never written), which stay inside the
 // allocation since the scale buffers and the fragments follow the ring.
 struct D2Smem {
-  size_t ring, slot, sbuf, shalf, xs, corr, scl, part, inbox, bars, total;
+  size_t ring, slot, sbuf, shalf, xs, corr, scl, xsum, part, inbox, bars, total;
 };
-__host__ __device__ inline D2Smem d2_smem(int B, int NT, int T, int H, int Gh, int sbox, int NS) {
+// zp: asymmetric groups, which also keep the plain group sums of x.
+__host__ __device__ inline D2Smem d2_smem(int B, int NT, int T, int H, int Gh, int sbox, int NS, bool zp = false) {
   D2Smem s{};
   auto al = [](size_t v, size_t a) { return (v + a - 1) / a * a; };
   s.slot = al(static_cast<size_t>(H) * 16 * B, 128);
@@ -204,14 +207,17 @@ __host__ __device__ inline D2Smem d2_smem(int B, int NT, int T, int H, int Gh, i
   s.xs = al(s.sbuf + 2 * s.shalf, 128);
   s.corr = s.xs + static_cast<size_t>(NT) * Gh * 4 * 32 * 16;
   s.scl = s.corr + static_cast<size_t>(NT) * 8 * Gh * 4;
-  s.part = al(s.scl + static_cast<size_t>(NT) * 8 * Gh * 4, 16);
+  s.xsum = s.scl + static_cast<size_t>(NT) * 8 * Gh * 4;
+  s.part = al(s.xsum + (zp ? static_cast<size_t>(NT) * 8 * Gh * 4 : 0), 16);
   s.inbox = s.part + static_cast<size_t>(T) * kTileRows * NT * 8 * 4;
   s.bars = al(s.inbox + static_cast<size_t>(T) * (kTileRows / 2) * NT * 8 * 4, 8);
   s.total = s.bars + (2 * kMaxStages + 6) * 8;
   return s;
 }
 
-// kMode 0: WNA16. kMode 1: W4A8 (x quantized per token in the staging).
+// kMode 0: WNA16. kMode 3: WNA16 with asymmetric groups (a zero point per
+// (row, group): the correction of a group grows by (zp - 2^(b-1)) sum x).
+// kMode 1: W4A8 (x quantized per token in the staging).
 // kMode 2: W4A8, and instead of y the exact per-group integer accumulators
 // acc[m, n, g] = sum_{k in g} xq[m, k] (q[n, k] - 8) are written (the test
 // and debug mode of the same main loop; the reduction and exchange still run).
@@ -219,7 +225,8 @@ template <int B, int NT, int kMode>
 __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const __grid_constant__ CUtensorMap smap,
                                                               const D2Params p) {
-  constexpr bool kQuant = kMode >= 1;
+  constexpr bool kQuant = kMode == 1 || kMode == 2;
+  constexpr bool kZp = kMode == 3;
   constexpr bool kF16 = uses_fp16<B>();
   constexpr int kTok = NT * 8;  // token columns of the partial-sum buffer
   extern __shared__ uint8_t smem_raw[];
@@ -232,12 +239,13 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   const int Gh = p.Gh, T = p.T, NS = p.NS, ksplit = p.ksplit, H = p.H;
-  const D2Smem L = d2_smem(B, NT, T, H, Gh, p.sbox, NS);
+  const D2Smem L = d2_smem(B, NT, T, H, Gh, p.sbox, NS, kZp);
   uint8_t* ring = base + L.ring;
   uint16_t* sbuf = reinterpret_cast<uint16_t*>(base + L.sbuf);
   uint4* xs4 = reinterpret_cast<uint4*>(base + L.xs);
   float* corr = reinterpret_cast<float*>(base + L.corr);
   float* scl = reinterpret_cast<float*>(base + L.scl);
+  float* xsm = reinterpret_cast<float*>(base + L.xsum);  // kZp: plain group sums of x
   float* part = reinterpret_cast<float*>(base + L.part);    // this CTA's sums, [T*32 rows][kTok]
   float* inbox = reinterpret_cast<float*>(base + L.inbox);  // the peer's sums of our half, [T*16][kTok]
   uint64_t* full = reinterpret_cast<uint64_t*>(base + L.bars);  // [kMaxStages]
@@ -260,11 +268,15 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
   const uint32_t scale_bytes = static_cast<uint32_t>(H) * p.sbox * 2u;
 
   if (threadIdx.x == 0) griddep_launch_dependents();
+  const uint64_t lim = c_wait_limit_ns;
 
   if (warp == kCWarps) {
-    // ---- producer: initialise the barriers, then stream at once; the
-    // consumers learn of the initialisation through named barrier 2, the
-    // peer CTA through the cluster barrier
+    // ---- producer: initialise the barriers, then stream at once. Shared
+    // memory still holds the barrier words of the previous kernel on this SM:
+    // the consumers learn of the initialisation through named barrier 2,
+    // which the producer only arrives on, after a CTA-scope release fence
+    // (they wait on it, then fence, before their first barrier operation);
+    // the peer CTA learns of it through the cluster barrier.
     if (lane == 0) {
       for (int s = 0; s < NS; ++s) {
         mbar_init(&full[s], 1);
@@ -278,10 +290,11 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
       mbar_init(&sfull[1], 1);
       s_abort = 0;
       fence_mbar_init();
+      asm volatile("fence.acq_rel.cta;" ::: "memory");
     }
     __syncwarp();
     cluster_arrive();
-    init_done_arrive();
+    asm volatile("bar.arrive 2, %0;" ::"n"(kThreads2) : "memory");
     // chunk k = rows r0 + k H .. + H - 1; stage = one group of this CTA's K
     // half; the chunk's first stage also brings its scale box
     if (lane == 0) {
@@ -289,7 +302,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
       bool stop = false;
       for (int k = 0; k < nck && !stop; ++k) {
         const int rc = static_cast<int>(r0 + static_cast<int64_t>(k) * H);
-        if (k >= 2 && !mbar_wait_bounded(&cdone[k & 1], ((k >> 1) - 1) & 1)) {
+        if (k >= 2 && !mbar_wait_bounded(&cdone[k & 1], ((k >> 1) - 1) & 1, lim)) {
           record_status(p.status, kStatusTimeout);
           s_abort = 1;
           break;
@@ -300,7 +313,11 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
         tma_load_2d(sbuf + (k & 1) * sbox_elems, &smap, scol0, rc, &sfull[k & 1]);
         for (int gl = 0; gl < Gh; ++gl, ++it) {
           const uint32_t s = it % NS;
-          if (s_abort || (it >= static_cast<uint32_t>(NS) && !mbar_wait_bounded(&empty[s], ((it / NS) - 1) & 1))) {
+          if (static_cast<int64_t>(it) == c_stop_stage) {  // test hook: stop issuing here
+            stop = true;
+            break;
+          }
+          if (s_abort || (it >= static_cast<uint32_t>(NS) && !mbar_wait_bounded(&empty[s], ((it / NS) - 1) & 1, lim))) {
             record_status(p.status, kStatusTimeout);
             s_abort = 1;
             stop = true;
@@ -339,6 +356,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
       for (int e = threadIdx.x; e < nz * Gh; e += kCWarps * 32) {
         corr[zt0 * Gh + e] = 0.0f;
         scl[zt0 * Gh + e] = 1.0f;
+        if constexpr (kZp) xsm[zt0 * Gh + e] = 0.0f;
       }
     }
     griddep_wait();
@@ -449,8 +467,8 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           }
         }
         uint32_t frag[16];
-        float cr, sb;
-        make_fragments<B>(xv, frag, cr, sb);  // every lane: it shuffles within its quad
+        float cr, sb, xsum;
+        make_fragments<B>(xv, frag, cr, sb, xsum);  // every lane: it shuffles within its quad
         if (valid) {
 #pragma unroll
           for (int i2 = 0; i2 < 4; ++i2)
@@ -459,12 +477,15 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           if (t == 0) {
             corr[tok * Gh + gl] = cr;
             scl[tok * Gh + gl] = sb;
+            if constexpr (kZp) xsm[tok * Gh + gl] = xsum;
           }
         }
       }
     }
     consumer_sync();
-    init_done_wait();  // the producer has initialised the barriers
+    // the producer has initialised the barriers (named barrier 2)
+    asm volatile("bar.sync 2, %0;" ::"n"(kThreads2) : "memory");
+    asm volatile("fence.acq_rel.cta;" ::: "memory");
 
     bool stop = false;  // warp-uniform
     uint32_t slot_cur = static_cast<uint32_t>(kr), phase_cur = 0;  // this warp's next stage: slot, phase
@@ -480,7 +501,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           for (int e = 0; e < 4; ++e) acc[j][h][e] = 0.0f;
 
       // the chunk's scales (every active warp waits on every chunk's phase)
-      if (active && !stop && !__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&sfull[k & 1], (k >> 1) & 1))) {
+      if (active && !stop && !__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&sfull[k & 1], (k >> 1) & 1, lim))) {
         if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
         s_abort = 1;
         stop = true;
@@ -492,12 +513,25 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           // stages advance by ksplit, which divides NS and Gh, so both are
           // carried along instead of divided out
           const uint32_t s = slot_cur, phase = phase_cur;
+          // kZp: the zero points of this thread's four rows in this group,
+          // loaded before the stage wait (global memory, so their latency
+          // overlaps it), as zp - 2^(b-1)
+          float zd[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          if constexpr (kZp) {
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const int64_t row = rc + rowt + 8 * qq;
+              if (row < r1)
+                zd[qq] = static_cast<float>(p.zeros[row * p.G + gbase + gl] & ((1u << B) - 1u)) -
+                         static_cast<float>(1 << (B - 1));
+            }
+          }
           slot_cur += static_cast<uint32_t>(ksplit);
           if (slot_cur >= static_cast<uint32_t>(NS)) {
             slot_cur -= static_cast<uint32_t>(NS);
             phase_cur ^= 1u;
           }
-          if (!__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&full[s], phase))) {
+          if (!__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&full[s], phase, lim))) {
             if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
             s_abort = 1;
             stop = true;
@@ -509,7 +543,13 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           load_slice<B>(st, rowt + 8, t, w1);
           load_slice<B>(st, rowt + 16, t, w2);
           load_slice<B>(st, rowt + 24, t, w3);
-          __syncwarp();  // every lane has its words: the slot may be refilled
+          // the slot may be refilled once every lane's reads are done: the
+          // refill is a TMA (async-proxy) write, which the generic-proxy reads
+          // above are ordered before only by a proxy fence in each reading
+          // thread (without it, a read still in flight could see the next
+          // stage's bytes)
+          fence_proxy_async_smem();
+          __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);
           const int scol = gbase + gl - scol0;
           float sc[4];
@@ -561,12 +601,26 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           for (int j = 0; j < NT; ++j) {
             const int ti0 = (j * 8 + 2 * t) * Gh + gl, ti1 = ti0 + Gh;
             const float cr0 = corr[ti0], cr1 = corr[ti1], sl0 = scl[ti0], sl1 = scl[ti1];
+            if constexpr (kZp) {
+              // rows rowt + 16 h (e = 0, 1) and rowt + 16 h + 8 (e = 2, 3)
+              const float x0 = xsm[ti0], x1 = xsm[ti1];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              acc[j][h][0] = fmaf(sc[2 * h], fmaf(sl0, c[j][h][0], -cr0), acc[j][h][0]);
-              acc[j][h][1] = fmaf(sc[2 * h], fmaf(sl1, c[j][h][1], -cr1), acc[j][h][1]);
-              acc[j][h][2] = fmaf(sc[2 * h + 1], fmaf(sl0, c[j][h][2], -cr0), acc[j][h][2]);
-              acc[j][h][3] = fmaf(sc[2 * h + 1], fmaf(sl1, c[j][h][3], -cr1), acc[j][h][3]);
+              for (int h = 0; h < 2; ++h) {
+                acc[j][h][0] = fmaf(sc[2 * h], fmaf(sl0, c[j][h][0], -fmaf(zd[2 * h], x0, cr0)), acc[j][h][0]);
+                acc[j][h][1] = fmaf(sc[2 * h], fmaf(sl1, c[j][h][1], -fmaf(zd[2 * h], x1, cr1)), acc[j][h][1]);
+                acc[j][h][2] =
+                    fmaf(sc[2 * h + 1], fmaf(sl0, c[j][h][2], -fmaf(zd[2 * h + 1], x0, cr0)), acc[j][h][2]);
+                acc[j][h][3] =
+                    fmaf(sc[2 * h + 1], fmaf(sl1, c[j][h][3], -fmaf(zd[2 * h + 1], x1, cr1)), acc[j][h][3]);
+              }
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                acc[j][h][0] = fmaf(sc[2 * h], fmaf(sl0, c[j][h][0], -cr0), acc[j][h][0]);
+                acc[j][h][1] = fmaf(sc[2 * h], fmaf(sl1, c[j][h][1], -cr1), acc[j][h][1]);
+                acc[j][h][2] = fmaf(sc[2 * h + 1], fmaf(sl0, c[j][h][2], -cr0), acc[j][h][2]);
+                acc[j][h][3] = fmaf(sc[2 * h + 1], fmaf(sl1, c[j][h][3], -cr1), acc[j][h][3]);
+              }
             }
           }
         }
@@ -576,7 +630,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
 
       // the peer has consumed its inbox of the previous chunk: it may be
       // written again
-      if (k >= 1 && !__all_sync(0xFFFFFFFFu, mbar_wait_cluster_bounded(dbar, (k - 1) & 1))) {
+      if (k >= 1 && !__all_sync(0xFFFFFFFFu, mbar_wait_cluster_bounded(dbar, (k - 1) & 1, lim))) {
         if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
         s_abort = 1;
         stop = true;
@@ -615,7 +669,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
       consumer_sync();
       if (threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(rbar), peer));
       // the peer's sums of our rows are in our inbox: combine, write y
-      const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait_cluster_bounded(rbar, k & 1));
+      const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait_cluster_bounded(rbar, k & 1, lim));
       if (!ready && threadIdx.x == 0) {
         record_status(p.status, kStatusTimeout);
         s_abort = 1;
@@ -638,7 +692,7 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
     // The pair leaves together: waiting for the peer's last arrival (measured:
     // letting each CTA leave as soon as its rows are written is slower when
     // the next kernel launches programmatically).
-    if (nck >= 1 && !mbar_wait_cluster_bounded(dbar, (nck - 1) & 1) && threadIdx.x == 0)
+    if (nck >= 1 && !mbar_wait_cluster_bounded(dbar, (nck - 1) & 1, lim) && threadIdx.x == 0)
       record_status(p.status, kStatusTimeout);
   }
   __syncthreads();
@@ -651,7 +705,7 @@ struct D2Plan {
   bool ok;
 };
 
-D2Plan make_d2plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
+D2Plan make_d2plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count, bool zp = false) {
   D2Plan pl{};
   pl.ok = false;
   // K % 1024 == 0: the scale rows are 16-byte multiples (TMA) and each K half
@@ -684,7 +738,7 @@ D2Plan make_d2plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
   for (int ks = kCWarps / p.T; ks >= 1 && p.NS == 0; --ks) {
     if (ks > p.Gh || p.Gh % ks != 0) continue;
     for (int ns = (kMaxStages / ks) * ks; ns >= ks && ns >= 2; ns -= ks) {
-      if (d2_smem(bits, pl.NT, p.T, p.H, p.Gh, p.sbox, ns).total <= kSmemCap) {
+      if (d2_smem(bits, pl.NT, p.T, p.H, p.Gh, p.sbox, ns, zp).total <= kSmemCap) {
         p.ksplit = ks;
         p.NS = ns;
         break;
@@ -692,7 +746,7 @@ D2Plan make_d2plan(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
     }
   }
   if (p.NS < 2 || p.ksplit < 1) return pl;
-  pl.smem = d2_smem(bits, pl.NT, p.T, p.H, p.Gh, p.sbox, p.NS).total + 1024;  // + base alignment
+  pl.smem = d2_smem(bits, pl.NT, p.T, p.H, p.Gh, p.sbox, p.NS, zp).total + 1024;  // + base alignment
   pl.ok = true;
   return pl;
 }
@@ -724,12 +778,13 @@ cudaError_t d2launch(const Ctx& c, const CUtensorMap& wmap, const CUtensorMap& s
 
 template <int kMode>
 cudaError_t d2launch_b(const Ctx& c, int bits, const CUtensorMap& wmap, const CUtensorMap& smap, const D2Plan& pl) {
-  if constexpr (kMode >= 1) {
+  if constexpr (kMode == 1 || kMode == 2) {
     if (bits != 4) return cudaErrorInvalidValue;
     return pl.NT == 1 ? d2launch<4, 1, kMode>(c, wmap, smap, pl) : d2launch<4, 2, kMode>(c, wmap, smap, pl);
   } else {
-#define WQ_D2(BB) \
-  case BB: return pl.NT == 1 ? d2launch<BB, 1, 0>(c, wmap, smap, pl) : d2launch<BB, 2, 0>(c, wmap, smap, pl);
+#define WQ_D2(BB)                                                                 \
+  case BB:                                                                        \
+    return pl.NT == 1 ? d2launch<BB, 1, kMode>(c, wmap, smap, pl) : d2launch<BB, 2, kMode>(c, wmap, smap, pl);
     switch (bits) {
       WQ_D2(2)
       WQ_D2(3)
@@ -746,8 +801,8 @@ cudaError_t d2launch_b(const Ctx& c, int bits, const CUtensorMap& wmap, const CU
 
 }  // namespace
 
-bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
-  return bits >= 2 && bits <= 8 && make_d2plan(M, N, K, bits, sm_count).ok;
+bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count, bool zp) {
+  return bits >= 2 && bits <= 8 && make_d2plan(M, N, K, bits, sm_count, zp).ok;
 }
 
 bool decode2_shape(int64_t M, int64_t K) { return M >= 1 && M <= 16 && K >= 1024 && K % 1024 == 0; }
@@ -756,14 +811,14 @@ bool decode2_shape(int64_t M, int64_t K) { return M >= 1 && M <= 16 && K >= 1024
 // configuration (ksplit 1, two ring slots) fits at the largest chunk any SM
 // count gives: a chunk has at most min(N, kMaxH) rows, and the shared-memory
 // footprint grows with the rows, the tiles and the ring depth.
-bool decode2_fits_any(int64_t M, int64_t N, int64_t K, int bits) {
+bool decode2_fits_any(int64_t M, int64_t N, int64_t K, int bits, bool zp) {
   if (bits < 2 || bits > 8 || !decode2_shape(M, K) || N < 1 || N >= (int64_t(1) << 31)) return false;
   const int G = static_cast<int>(K / 128), Gh = G / 2;
   const int sx0 = (Gh / 8) * 8, sbox = ((G - sx0 + 7) / 8) * 8;
   if (sbox < Gh || sbox > 256) return false;
   const int H = static_cast<int>(N < kMaxH ? N : kMaxH);
   const int T = (H + kTileRows - 1) / kTileRows;
-  return d2_smem(bits, M <= 8 ? 1 : 2, T, H, Gh, sbox, 2).total <= kSmemCap;
+  return d2_smem(bits, M <= 8 ? 1 : 2, T, H, Gh, sbox, 2, zp).total <= kSmemCap;
 }
 
 int decode2_plan_info(int64_t M, int64_t N, int64_t K, int bits, int sm_count, int64_t* out) {
@@ -778,14 +833,16 @@ int decode2_plan_info(int64_t M, int64_t N, int64_t K, int bits, int sm_count, i
 cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a) {
   // the W4A8 modes here take a.x, the bf16 activations, and quantize them per
   // token in the kernel; kW4a8GroupAcc writes a.acc instead of a.y
-  const int mode = a.mode == GemvMode::kWna16 ? 0 : a.mode == GemvMode::kW4a8 ? 1 : 2;
+  const bool zp = a.mode == GemvMode::kWna16 && a.zeros != nullptr;
+  const int mode = a.mode == GemvMode::kWna16 ? (zp ? 3 : 0) : a.mode == GemvMode::kW4a8 ? 1 : 2;
   if (a.x == nullptr || (mode == 2 && a.acc == nullptr)) return cudaErrorInvalidValue;
-  const D2Plan pl = make_d2plan(a.M, a.N, a.K, a.bits, c.sm_count);
+  const D2Plan pl = make_d2plan(a.M, a.N, a.K, a.bits, c.sm_count, zp);
   if (!pl.ok) return cudaErrorInvalidValue;
   D2Plan q = pl;
   q.prm.x = a.x;
   q.prm.y = a.y;
   q.prm.acc = a.acc;
+  q.prm.zeros = a.zeros;
   q.prm.status = c.status;
   CUtensorMap wmap, smap;
   const uint64_t words = static_cast<uint64_t>(a.K) * a.bits / 32;
@@ -797,7 +854,21 @@ cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a) {
     return cudaErrorInvalidValue;
   if (mode == 1) return d2launch_b<1>(c, a.bits, wmap, smap, q);
   if (mode == 2) return d2launch_b<2>(c, a.bits, wmap, smap, q);
+  if (mode == 3) return d2launch_b<3>(c, a.bits, wmap, smap, q);
   return d2launch_b<0>(c, a.bits, wmap, smap, q);
 }
 
 }  // namespace wq
+
+extern "C" wq_status wq_debug_decode_wait_fault(int64_t stop_stage, uint64_t wait_limit_ns) {
+  using namespace wq;
+  const uint64_t lim = wait_limit_ns == 0 ? kWaitLimitNs : wait_limit_ns;
+  const int64_t stage = stop_stage < 0 ? -1 : stop_stage;
+  cudaError_t e = cudaMemcpyToSymbol(c_wait_limit_ns, &lim, sizeof(lim));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(c_stop_stage, &stage, sizeof(stage));
+  if (e != cudaSuccess) {
+    set_error("wq_debug_decode_wait_fault: %s", cudaGetErrorString(e));
+    return WQ_ECUDA;
+  }
+  return WQ_OK;
+}

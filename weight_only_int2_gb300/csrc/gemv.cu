@@ -62,6 +62,7 @@ struct Params {
   const int8_t* xq;
   const float* sx;
   const uint16_t* scales;
+  const uint8_t* zeros;  // asymmetric groups (kWna16): [N, G], or null
   int64_t M, N, K;
   int G;     // groups along K
   int gper;  // groups per split
@@ -81,7 +82,7 @@ struct Params {
 // ---------------------------------------------------------------------------
 template <int B, int NT, int MODE>
 __device__ __forceinline__ void stage_x(const Params& p, int64_t m0, int gabs0, int nc, uint4* xs4,
-                                        float* corr, float* scl) {
+                                        float* corr, float* scl, float* xsm) {
   constexpr int XC = kXGroupsTimesNT / NT;
   constexpr int kJobs = NT * XC * 32;
   static_assert(kJobs % kThreads == 0, "staging jobs must divide evenly");
@@ -99,8 +100,8 @@ __device__ __forceinline__ void stage_x(const Params& p, int64_t m0, int gabs0, 
     float v[32];
     load_slice_x<kInt8>(src, valid, v);
     uint32_t frag[16];
-    float cr, sb;
-    make_fragments<B>(v, frag, cr, sb);
+    float cr, sb, xsum;
+    make_fragments<B>(v, frag, cr, sb, xsum);
 #pragma unroll
     for (int i2 = 0; i2 < 4; ++i2)
       xs4[((j * XC + gi) * 4 + i2) * 32 + ln] =
@@ -109,6 +110,7 @@ __device__ __forceinline__ void stage_x(const Params& p, int64_t m0, int gabs0, 
       const int tokl = j * 8 + (ln >> 2);
       corr[tokl * XC + gi] = cr;
       scl[tokl * XC + gi] = sb;
+      xsm[tokl * XC + gi] = xsum;
     }
   }
 }
@@ -126,8 +128,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
   uint4* xs4 = reinterpret_cast<uint4*>(smem + kWarps * kStages * kStageBytes);
   float* corr = reinterpret_cast<float*>(xs4 + NT * XC * 4 * 32);
   float* scl = corr + NT * 8 * XC;
-  uint64_t* bars_all = reinterpret_cast<uint64_t*>(scl + NT * 8 * XC);
+  float* xsm = scl + NT * 8 * XC;  // plain group sums of x (asymmetric groups)
+  uint64_t* bars_all = reinterpret_cast<uint64_t*>(xsm + NT * 8 * XC);
   uint16_t* ssm = reinterpret_cast<uint16_t*>(bars_all + kWarps * kStages);  // [128][gper]
+  uint8_t* zsm = reinterpret_cast<uint8_t*>(ssm + kRowsPerCta * p.gper);      // [128][gper] zero points
   __shared__ int s_last;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -159,8 +163,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
       const int r = idx / ngroups, gi = idx - r * ngroups;
       const int64_t row = rb0 + r;
       ssm[r * p.gper + gi] = (row < p.N) ? p.scales[row * p.G + gbeg + gi] : static_cast<uint16_t>(0);
+      if (p.zeros != nullptr)
+        zsm[r * p.gper + gi] = (row < p.N) ? p.zeros[row * p.G + gbeg + gi] : static_cast<uint8_t>(0);
     }
   }
+  constexpr float kZero = static_cast<float>(1 << (B - 1));
+  constexpr uint32_t kZMask = (1u << B) - 1u;
 
   const int rl_g = warp * kRowsPerWarp + g;  // local index of this thread's first row
   const int64_t r_g = row0 + g, r_g8 = row0 + g + 8;
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     const int nc = min(XC, ngroups - cb);
     const int gabs0 = gbeg + cb;
     __syncthreads();  // previous chunk fully consumed (and scales written)
-    stage_x<B, NT, MODE>(p, m0, gabs0, nc, xs4, corr, scl);
+    stage_x<B, NT, MODE>(p, m0, gabs0, nc, xs4, corr, scl, xsm);
     __syncthreads();
 
     if (!warp_active) {
@@ -222,12 +230,23 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
           mma16<kF16>(c1, ra[4 * i2 + 2], rb[4 * i2 + 2], ra[4 * i2 + 3], rb[4 * i2 + 3], bv.z, bv.w);
         }
         const int tl0 = j * 8 + 2 * t;
-        const float cr0 = corr[tl0 * XC + gi], cr1 = corr[(tl0 + 1) * XC + gi];
+        float cr0 = corr[tl0 * XC + gi], cr1 = corr[(tl0 + 1) * XC + gi];
+        float cr2 = cr0, cr3 = cr1;
         const float sc0 = scl[tl0 * XC + gi], sc1 = scl[(tl0 + 1) * XC + gi];
+        if (MODE == static_cast<int>(GemvMode::kWna16) && p.zeros != nullptr) {
+          // asymmetric groups: the correction carries (zp - 2^(b-1)) sum x
+          const float zd_g = static_cast<float>(zsm[rl_g * p.gper + it] & kZMask) - kZero;
+          const float zd_g8 = static_cast<float>(zsm[(rl_g + 8) * p.gper + it] & kZMask) - kZero;
+          const float x0 = xsm[tl0 * XC + gi], x1 = xsm[(tl0 + 1) * XC + gi];
+          cr2 = fmaf(zd_g8, x0, cr0);
+          cr3 = fmaf(zd_g8, x1, cr1);
+          cr0 = fmaf(zd_g, x0, cr0);
+          cr1 = fmaf(zd_g, x1, cr1);
+        }
         const float d0 = fmaf(sc0, c0[0] + c1[0], -cr0);
         const float d1 = fmaf(sc1, c0[1] + c1[1], -cr1);
-        const float d2 = fmaf(sc0, c0[2] + c1[2], -cr0);
-        const float d3 = fmaf(sc1, c0[3] + c1[3], -cr1);
+        const float d2 = fmaf(sc0, c0[2] + c1[2], -cr2);
+        const float d3 = fmaf(sc1, c0[3] + c1[3], -cr3);
         if constexpr (MODE == static_cast<int>(GemvMode::kW4a8GroupAcc)) {
           const int64_t tk0 = m0 + tl0, tk1 = tk0 + 1;
           const int64_t G = p.G;
@@ -307,9 +326,9 @@ size_t smem_bytes(int gper) {
   constexpr int XC = kXGroupsTimesNT / NT;
   return static_cast<size_t>(kWarps) * kStages * kRowsPerWarp * 16 * B      // weight stages
          + static_cast<size_t>(NT) * XC * 4 * 32 * 16                       // B fragments
-         + static_cast<size_t>(NT) * 8 * XC * 4 * 2                         // corrections, scales
+         + static_cast<size_t>(NT) * 8 * XC * 4 * 3                         // corrections, scales, sums
          + static_cast<size_t>(kWarps) * kStages * 8                        // mbarriers
-         + ((static_cast<size_t>(kRowsPerCta) * gper * 2 + 15) / 16) * 16;  // group scales
+         + ((static_cast<size_t>(kRowsPerCta) * gper * 3 + 15) / 16) * 16;  // group scales, zero points
 }
 
 struct Plan {
@@ -404,6 +423,7 @@ cudaError_t launch_gemv(const Ctx& c, const GemvArgs& a) {
   prm.xq = a.xq;
   prm.sx = a.sx;
   prm.scales = a.scales;
+  prm.zeros = a.mode == GemvMode::kWna16 ? a.zeros : nullptr;
   prm.M = a.M;
   prm.N = a.N;
   prm.K = a.K;

@@ -29,7 +29,8 @@
 //               16*b bytes] per load.
 //   warps 3-18  four teams of 4 warps; team j takes every fourth stage. A
 //               thread turns the 64 codes of one weight row into bf16
-//               RN(s * (q - z)) (q - z exact, one rounding) and writes them
+//               RN(s * (q - z)) (q - z exact, one rounding; z = 2^(b-1), or
+//               the group's zero point for asymmetric groups) and writes them
 //               to its TMEM lane (tcgen05.st). The same warps read the
 //               accumulator out after each tile (tcgen05.ld), release it,
 //               and store bf16 outputs.
@@ -86,6 +87,7 @@ struct Layout {
 
 struct PParams {
   const uint16_t* scales;  // bf16 [N, G]
+  const uint8_t* zeros;    // asymmetric groups: zero points [N, G], or null (2^(b-1))
   int64_t M, N, K;
   int G;
   int row_tiles, tok_tiles;  // ceil(N / 128), ceil(M / TN)
@@ -98,6 +100,7 @@ using namespace tc;
 // ---- dequantization: wq_dequant.cuh -----------------------------------------
 
 using dq::dequant_slice;
+using dq::dequant_slice_zp;
 
 template <int B, int TN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -251,11 +254,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the scale of the next group this thread dequantizes, loaded one use ahead
     int nt = first, ng = gpar;
     while (ng >= G && nt < ntiles) ng -= G, nt += step;
-    auto load_scale = [&]() -> uint16_t {
-      uint16_t v = 0;
+    // the scale bits and (asymmetric groups) the zero point of that group,
+    // as scale | zero << 16
+    auto load_scale = [&]() -> uint32_t {
+      uint32_t v = 0;
       if (nt < ntiles) {
         const int64_t row = static_cast<int64_t>(nt % p.row_tiles) * kBM + r;
-        if (row < p.N) v = p.scales[row * G + ng];
+        if (row < p.N) {
+          v = p.scales[row * G + ng];
+          if (p.zeros != nullptr) v |= static_cast<uint32_t>(p.zeros[row * G + ng]) << 16;
+        }
       }
       ng += 2;
       while (ng >= G && nt < ntiles) ng -= G, nt += step;
@@ -296,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    uint16_t sb = load_scale();
+    uint32_t sb = load_scale();
     uint32_t gi = 0;    // groups of the CTA's sequence
     int pend_k = -1, pend_t = 0;  // tile whose accumulator this warp has not read yet
     bool stop = false;  // warp-uniform
@@ -326,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           stop = true;
           break;
         }
-        const uint32_t s2 = static_cast<uint32_t>(sb) | (static_cast<uint32_t>(sb) << 16);
+        const uint32_t s2 = (sb & 0xFFFFu) | (sb << 16);
+        const uint32_t zc2 = dq::zero_pair<B>(sb >> 16);
         sb = load_scale();
         uint32_t w[2 * B];
         const uint8_t* prow = ps + pslot * L::kPSlot + r * 16 * B;
@@ -347,7 +356,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t wsl[B], os[16];
 #pragma unroll
           for (int j = 0; j < B; ++j) wsl[j] = w[half * B + j];
-          dequant_slice<B>(wsl, s2, os);
+          if (p.zeros != nullptr) {
+            dequant_slice_zp<B>(wsl, s2, zc2, os);
+          } else {
+            dequant_slice<B>(wsl, s2, os);
+          }
 #pragma unroll
           for (int j = 0; j < 16; ++j) o[16 * half + j] = os[j];
         }
@@ -422,7 +435,7 @@ bool prefill_supported(int64_t M, int64_t N, int64_t K, int bits) {
 }
 
 cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* packed, const uint16_t* scales,
-                           int64_t M, int64_t N, int64_t K, int bits, uint16_t* y) {
+                           int64_t M, int64_t N, int64_t K, int bits, uint16_t* y, const uint8_t* zeros) {
   const int tn = prefill_tile_tokens(M);
   CUtensorMap xmap, wmap;
   if (!make_tmap_bf16_2d_sw128(&xmap, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBK,
@@ -435,6 +448,7 @@ cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* pack
     return cudaErrorInvalidValue;
   PParams prm{};
   prm.scales = scales;
+  prm.zeros = zeros;
   prm.M = M;
   prm.N = N;
   prm.K = K;

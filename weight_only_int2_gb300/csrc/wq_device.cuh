@@ -81,17 +81,18 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
 }
 
 // Waits for the phase with the given parity to complete. Returns false if the
-// wait gave up after kWaitLimitNs; the caller then records the error and
-// leaves its loop instead of hanging the GPU. The deadline is checked every
-// 64 attempts, each of which may park the warp for up to 20 us.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// wait gave up after limit_ns (kWaitLimitNs unless a kernel passes its own);
+// the caller then records the error and leaves its loop instead of hanging the
+// GPU. The deadline is checked every 64 attempts, each of which may park the
+// warp for up to 20 us.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

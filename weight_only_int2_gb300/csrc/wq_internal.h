@@ -89,6 +89,7 @@ struct GemvArgs {
   const float* sx;     // kW4a8: per-token scale [M]
   const uint32_t* packed;
   const uint16_t* scales;
+  const uint8_t* zeros;  // kWna16, asymmetric groups: zero points [N, K/128], or null
   int64_t M, N, K;
   int bits;
   uint16_t* y;         // bf16 [M, N] (kWna16, kW4a8)
@@ -113,8 +114,10 @@ cudaError_t launch_decode(const Ctx& c, const GemvArgs& a);
 // Tensor-core GEMM for many tokens (tcgen05, dequantize-then-multiply).
 constexpr int64_t kPrefillMinTokens = 65;
 bool prefill_supported(int64_t M, int64_t N, int64_t K, int bits);
+// zeros: asymmetric groups, uint8 [N, K/128] zero points (low `bits` bits
+// used), or nullptr for the symmetric zero point 2^(bits-1).
 cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* packed, const uint16_t* scales,
-                           int64_t M, int64_t N, int64_t K, int bits, uint16_t* y);
+                           int64_t M, int64_t N, int64_t K, int bits, uint16_t* y, const uint8_t* zeros);
 
 // W4A8 on the tensor cores with exact per-group integer accumulation
 // (w4a8tc.cu): xqb holds the per-token int8 codes as bf16 values [M, K] and sx
@@ -141,11 +144,12 @@ inline bool use_prefill(int64_t M, int64_t N, int64_t K, int bits, int sm_count)
 // activations, which the kernel quantizes per token itself.
 bool decode2_shape(int64_t M, int64_t K);
 // Whether the pair kernel takes this shape whatever the device's SM count (>= 2).
-bool decode2_fits_any(int64_t M, int64_t N, int64_t K, int bits);
+// zp: asymmetric groups (the plan also keeps the plain group sums of x).
+bool decode2_fits_any(int64_t M, int64_t N, int64_t K, int bits, bool zp = false);
 // The CTA-pair decode plan for a shape, for host-side checks: out[14] =
 // {ok, C, H, nchunk, T, ksplit, NS, G, Gh, sbox, sx0, NT, smem bytes, max ring slots}.
 int decode2_plan_info(int64_t M, int64_t N, int64_t K, int bits, int sm_count, int64_t* out);
-bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count);
+bool decode2_supported(int64_t M, int64_t N, int64_t K, int bits, int sm_count, bool zp = false);
 cudaError_t launch_decode2(const Ctx& c, const GemvArgs& a);
 
 // The kernel a GEMM call launches, by shape (host only). The entry points
@@ -163,6 +167,15 @@ inline Route route_stream(int64_t M, int64_t N, int64_t K, int bits, int sm_coun
 inline Route route_wna16(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
   if (use_prefill(M, N, K, bits, sm_count)) return Route::kTensorCore;
   return route_stream(M, N, K, bits, sm_count, true);
+}
+
+// Asymmetric groups (a zero point per row and group): the kernels of
+// route_wna16 but the persistent split-K decode kernel, which has no
+// zero-point mode; the chunked kernel takes those shapes (K <= 16384).
+inline Route route_wna16_zp(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
+  if (use_prefill(M, N, K, bits, sm_count)) return Route::kTensorCore;
+  if (decode2_supported(M, N, K, bits, sm_count, true)) return Route::kDecodePair;
+  return gemv_supported(K) ? Route::kChunked : Route::kNone;
 }
 
 // W4A8: the pair kernel quantizes few tokens itself; for many tokens the codes
@@ -206,6 +219,14 @@ inline size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits) 
   return a > b ? a : b;
 }
 
+// The same query for asymmetric groups (route_wna16_zp): no split-K decode
+// kernel, and the pair kernel's plan keeps the group sums of x as well.
+inline size_t stream_workspace_bytes_zp(int64_t M, int64_t N, int64_t K, int bits) {
+  if (M >= kPrefillMinTokens && prefill_supported(M, N, K, bits)) return 0;
+  if (decode2_fits_any(M, N, K, bits, true)) return 0;
+  return gemv_workspace_bytes(M, N, K);
+}
+
 // ---- the WNA16 entry point in steps (api.cu), shared by wna16_gemm and the
 // allocation-free variant so that both validate and route identically ----
 
@@ -218,9 +239,12 @@ wq_status wna16_check_args(const uint16_t* x, int64_t M, const uint32_t* Wpacked
 bool maybe_tensor_core(int64_t M, int64_t N, int64_t K, int bits);
 // The device context and the kernel the shape takes (device queries, no
 // launch); WQ_EUNSUPPORTED when no kernel takes it.
-wq_status wna16_route(int64_t M, int64_t N, int64_t K, int bits, void* stream, Ctx* c, Route* r);
-// Launches route r (arguments already checked; workspace as the route needs).
+// zp: the call has zero points (route_wna16_zp).
+wq_status wna16_route(int64_t M, int64_t N, int64_t K, int bits, void* stream, Ctx* c, Route* r, bool zp = false);
+// Launches route r (arguments already checked; workspace as the route needs;
+// zeros null for symmetric groups).
 wq_status wna16_launch(const Ctx& c, Route r, const uint16_t* x, int64_t M, const uint32_t* Wpacked,
-                 const uint16_t* scales, int64_t N, int64_t K, int bits, uint16_t* y, void* workspace);
+                       const uint16_t* scales, int64_t N, int64_t K, int bits, uint16_t* y, void* workspace,
+                       const uint8_t* zeros = nullptr);
 
 }  // namespace wq

@@ -188,7 +188,7 @@ __device__ __forceinline__ void load_slice_x(const void* src, bool valid, float 
 
 template <int B>
 __device__ __forceinline__ void make_fragments(const float (&v)[32], uint32_t (&frag)[16], float& corr,
-                                               float& scale_back) {
+                                               float& scale_back, float& xsum) {
   constexpr bool kF16 = uses_fp16<B>();
   constexpr float kMagic = kF16 ? 1024.0f : 128.0f;
   constexpr float kZero = static_cast<float>(1 << (B - 1));
@@ -228,6 +228,15 @@ __device__ __forceinline__ void make_fragments(const float (&v)[32], uint32_t (&
   sum_o += __shfl_xor_sync(0xFFFFFFFFu, sum_o, 1);
   sum_o += __shfl_xor_sync(0xFFFFFFFFu, sum_o, 2);
   corr = fmaf(kMagic, sum_o, kZero * sum);
+  xsum = sum;
+}
+
+// The same without the plain group sum (symmetric groups only).
+template <int B>
+__device__ __forceinline__ void make_fragments(const float (&v)[32], uint32_t (&frag)[16], float& corr,
+                                               float& scale_back) {
+  float xsum;
+  make_fragments<B>(v, frag, corr, scale_back, xsum);
 }
 
 }  // namespace unpack
