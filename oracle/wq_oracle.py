@@ -206,6 +206,36 @@ def wna16_zp_ref(x_bits, codes, scales_bits, zeros, bits: int, group: int = GROU
 
 
 # --------------------------------------------------------------------------
+# Mixture of experts: a WNA16 layer per expert over its own tokens
+# --------------------------------------------------------------------------
+# Model card "Qwen3.8-27B-INT6-Mixed-AutoRound", section "Findings", third
+# bullet: the serving path of the pages has no fused mixture-of-experts
+# WNA16 GEMM at 5/6/7 bits (its MoE method accepts only 4 and 8). The page
+# does not describe the grouped layer; the reading adopted here is the plain
+# one: the tokens come sorted by expert, expert e owns token rows
+# [offsets[e], offsets[e+1]) and applies its own layer (codes [N, K], scales
+# [N, K // 128]) to them.
+
+def moe_ref(x_bits, offsets, codes, scales_bits, bits: int, group: int = GROUP) -> np.ndarray:
+    """y[offsets[e]:offsets[e+1]] = wna16_ref(x[offsets[e]:offsets[e+1]], W_e)
+    for each expert e; codes [E, N, K], scales [E, N, K // group]."""
+    off = [int(v) for v in np.asarray(offsets).reshape(-1)]
+    c = np.asarray(codes)
+    E, N, K = c.shape
+    if len(off) != E + 1 or off[0] != 0 or any(off[i] > off[i + 1] for i in range(E)):
+        raise ValueError("offsets must be E + 1 nondecreasing values starting at 0")
+    M = np.asarray(x_bits).shape[0]
+    if off[E] != M:
+        raise ValueError("offsets[E] must equal the number of token rows")
+    y = np.zeros((M, N), dtype=np.float64)
+    for e in range(E):
+        if off[e + 1] > off[e]:
+            y[off[e]:off[e + 1]] = wna16_ref(np.asarray(x_bits)[off[e]:off[e + 1]], c[e],
+                                             np.asarray(scales_bits)[e], bits, group)
+    return y
+
+
+# --------------------------------------------------------------------------
 # W4A8: per-token int8 activation quantization and integer accumulation
 # --------------------------------------------------------------------------
 

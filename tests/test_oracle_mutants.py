@@ -54,6 +54,9 @@ def _pin_calls():
         calls.append((f"zp closed form b{b}", P.test_zp_closed_form_constant_codes, (b,)))
         calls.append((f"zp at half range b{b}", P.test_zp_at_half_range_is_the_symmetric_layer, (b,)))
     calls.append(("zp shift invariance", P.test_zp_shift_invariance, ()))
+    calls.append(("moe brute force", P.test_moe_brute_force_exact_rationals, ()))
+    calls.append(("moe dense reductions", P.test_moe_with_one_expert_or_equal_experts_is_the_dense_layer, ()))
+    calls.append(("moe row order", P.test_moe_rows_follow_their_expert, ()))
     calls.append(("zp low bits", P.test_zp_uses_the_low_bits_of_each_byte, ()))
     return calls
 
@@ -310,7 +313,27 @@ def _zp_bits_masked_wrong(zeros, bits):
     return np.asarray(zeros).astype(np.int64) & ((1 << (int(bits) - 1)) - 1)
 
 
+def _moe_variant(kind):
+    def f(x_bits, offsets, codes, scales_bits, bits, group=W.GROUP):
+        off = [int(v) for v in np.asarray(offsets).reshape(-1)]
+        c = np.asarray(codes)
+        E, N, K = c.shape
+        M = np.asarray(x_bits).shape[0]
+        y = np.zeros((M, N), dtype=np.float64)
+        for e in range(E):
+            we = (e + 1) % E if kind == "next expert" else e
+            lo, hi = off[e], off[e + 1]
+            if kind == "first token dropped":
+                lo = min(lo + 1, hi)
+            if hi > lo:
+                y[lo:hi] = W.wna16_ref(np.asarray(x_bits)[lo:hi], c[we], np.asarray(scales_bits)[we], bits, group)
+        return y
+    return f
+
+
 MUTANTS = {
+    "MoE tokens use the next expert's weights": {"moe_ref": _moe_variant("next expert")},
+    "MoE expert ranges start one token late": {"moe_ref": _moe_variant("first token dropped")},
     "zero point per group ignored": {"dequant_zp": _dequant_zp_variant("ignored")},
     "zero point added instead of subtracted": {"dequant_zp": _dequant_zp_variant("added")},
     "zero point indexed k mod G": {"dequant_zp": _dequant_zp_variant("tiled")},

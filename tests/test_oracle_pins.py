@@ -520,3 +520,56 @@ def test_zp_uses_the_low_bits_of_each_byte():
     high = (zp | np.uint8(0xE0)).astype(np.uint8)                          # bits 5..7 set
     assert np.array_equal(O.wna16_zp_ref(x, q, s, high, bits), O.wna16_zp_ref(x, q, s, zp, bits))
     assert O.zero_points_used(np.array([0xFF], dtype=np.uint8), 5)[0] == 31
+
+
+# ---------------------------------------------------------------- mixture of experts
+
+def _moe_case(E, N, K, bits, counts, seed):
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    M = int(off[-1])
+    x = I.make_x(M, K, seed)
+    q = np.stack([I.make_codes(N, K, bits, seed + 1 + e) for e in range(E)])
+    s = np.stack([I.make_scales(N, K // 128, seed + 50 + e) for e in range(E)])
+    return off, x, q, s
+
+
+def test_moe_brute_force_exact_rationals():
+    """Three experts, ragged token counts including an empty expert: every
+    output against exact rational arithmetic with that token's expert."""
+    bits, N, K = 6, 3, 128
+    off, x, q, s = _moe_case(4, N, K, bits, [2, 0, 1, 2], 400)
+    y = O.moe_ref(x, off, q, s, bits)
+    z = 1 << (bits - 1)
+    for m in range(x.shape[0]):
+        e = int(np.searchsorted(off, m, side="right")) - 1
+        for n in range(N):
+            exact = sum(_frac_bf16(x[m, k]) * _frac_bf16(s[e, n, k // 128]) * (int(q[e, n, k]) - z)
+                        for k in range(K))
+            mag = sum(abs(_frac_bf16(x[m, k]) * _frac_bf16(s[e, n, k // 128]) * (int(q[e, n, k]) - z))
+                      for k in range(K))
+            assert abs(Fraction(float(y[m, n])) - exact) <= mag * Fraction(1, 2**45)
+
+
+def test_moe_with_one_expert_or_equal_experts_is_the_dense_layer():
+    bits, N, K = 5, 7, 256
+    off, x, q, s = _moe_case(1, N, K, bits, [9], 410)
+    assert np.array_equal(O.moe_ref(x, off, q, s, bits), O.wna16_ref(x, q[0], s[0], bits))
+    off, x, q, s = _moe_case(3, N, K, bits, [4, 1, 3], 420)
+    qe = np.repeat(q[:1], 3, axis=0)
+    se = np.repeat(s[:1], 3, axis=0)
+    assert np.array_equal(O.moe_ref(x, off, qe, se, bits), O.wna16_ref(x, q[0], s[0], bits))
+
+
+def test_moe_rows_follow_their_expert():
+    """Reordering the experts together with their token blocks permutes the
+    output rows the same way."""
+    bits, N, K = 7, 5, 256
+    counts = [3, 1, 4]
+    off, x, q, s = _moe_case(3, N, K, bits, counts, 430)
+    y = O.moe_ref(x, off, q, s, bits)
+    perm = [2, 0, 1]
+    blocks = [np.arange(off[e], off[e + 1]) for e in range(3)]
+    rows = np.concatenate([blocks[e] for e in perm])
+    off2 = np.concatenate([[0], np.cumsum([counts[e] for e in perm])])
+    y2 = O.moe_ref(x[rows], off2, q[perm], s[perm], bits)
+    assert np.array_equal(y2, y[rows])
