@@ -134,6 +134,28 @@ wq_status wna16_gemm_zp(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, co
  * wna16_workspace_bytes). */
 size_t wna16_zp_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits);
 
+/* Mixture-of-experts WNA16 layer, all experts in one launch [CARD "Findings",
+ * third bullet: the pages' serving path has no fused MoE WNA16 GEMM at 5/6/7
+ * bits]. The tokens come sorted by expert: expert e owns token rows
+ * [expert_offsets[e], expert_offsets[e+1]) of x and y and applies its own
+ * layer to them,
+ *   y[m, n] = sum_k x[m, k] * s_e[n, k/128] * (q_e[n, k] - 2^(bits-1)).
+ *  x              [M, K] bf16, tokens sorted by expert.
+ *  expert_offsets [E + 1] int32 DEVICE array (4-byte aligned): 0, ..., M,
+ *                 nondecreasing; the kernel clamps each value into [0, M] and
+ *                 to at least the previous one, so no offsets can make it
+ *                 read or write outside x and y (tokens outside every range
+ *                 are then left unwritten).
+ *  Wpacked        [E * N, ceil(K*bits/32)] uint32: the E layers' packed rows
+ *                 stacked (v1 layout); scales [E * N, K/128] bf16 likewise.
+ *  y              [M, N] bf16 output.
+ *  1 <= E <= 1024, E * N < 2^31, bits in 2..8. Runs on the tensor-core
+ *  kernel whatever the token counts (tiles of 128 or 256 tokens of one
+ *  expert); needs no workspace. */
+wq_status wna16_moe_gemm(const wq_bf16* x, int64_t M, const int32_t* expert_offsets, int64_t E,
+                         const uint32_t* Wpacked, const wq_bf16* scales, int64_t N, int64_t K, int bits, int group,
+                         wq_bf16* y, void* stream);
+
 /* WNA16 linear layer without a workspace argument, for callers that cannot
  * allocate device memory (no counterpart on the source pages; it is a
  * packaging of wna16_gemm). A serving engine that has reserved nearly all

@@ -26,6 +26,7 @@ from ._lib import (  # noqa: F401
     wna16_gemm,
     wna16_gemm_noalloc,
     wna16_gemm_zp,
+    wna16_moe_gemm,
     wna16_repack,
     wna16_workspace_bytes,
     wna16_zp_workspace_bytes,

@@ -34,6 +34,8 @@ SIGNATURES = {
     "wna16_gemm_zp": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_int, _c_int, _c_ptr,
                                _c_ptr, _c_size, _c_ptr]),
     "wna16_zp_workspace_bytes": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int]),
+    "wna16_moe_gemm": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_i64, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_int, _c_int,
+                                _c_ptr, _c_ptr]),
     "wna16_gemm_noalloc": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_int, _c_int,
                                     _c_ptr, _c_ptr]),
     "act_quant_int8": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr, _c_ptr]),
@@ -245,6 +247,24 @@ def wna16_gemm_zp(x: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor, z
     _check(load().wna16_gemm_zp(_ptr(x), M, _ptr(packed), _ptr(scales), _ptr(zeros), N, K, bits, group, _ptr(y),
                                 _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _stream()),
            "wna16_gemm_zp")
+    return y
+
+
+def wna16_moe_gemm(x: torch.Tensor, expert_offsets: torch.Tensor, packed: torch.Tensor, scales: torch.Tensor,
+                   E: int, N: int, K: int, bits: int, group: int = 128, y: torch.Tensor | None = None):
+    """Mixture of experts: x [M, K] sorted by expert, expert_offsets int32
+    [E + 1] on the device, packed [E * N, words] and scales [E * N, K/128]
+    stacked per expert; y [M, N]."""
+    M = x.shape[0]
+    _need(x, "x", torch.bfloat16, (M, K))
+    _need(expert_offsets, "expert_offsets", torch.int32, (E + 1,))
+    _need(packed, "packed", torch.int32, (E * N, packed_words_per_row(K, bits)))
+    _need(scales, "scales", torch.bfloat16, (E * N, K // group))
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", torch.bfloat16, (M, N))
+    _check(load().wna16_moe_gemm(_ptr(x), M, _ptr(expert_offsets), E, _ptr(packed), _ptr(scales), N, K, bits, group,
+                                 _ptr(y), _stream()), "wna16_moe_gemm")
     return y
 
 

@@ -86,6 +86,8 @@ wq_status check_bits(int bits) {
 
 // Sizes become grid dimensions and 32-bit TMA coordinates: all below 2^31.
 constexpr int64_t kMaxDim = 0x7FFFFFFF;
+// Experts of one grouped call (each tile looks its expert up in the offsets).
+constexpr int kMaxExperts = 1024;
 
 wq_status check_group_k(int group, int64_t K, const char* kname) {
   if (group != 128) return fail(WQ_EUNSUPPORTED, "group must be 128 (got %d)", group);
@@ -338,6 +340,29 @@ wq_status wna16_gemm_zp(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, co
   const size_t need_r = route_workspace_bytes(r, M, N, K);
   if (need_r > 0) WQ_TRY(check_workspace(workspace, ws_bytes, need_r));
   return wna16_launch(c, r, x, M, Wpacked, scales, N, K, bits, y, workspace, zeros);
+}
+
+wq_status wna16_moe_gemm(const wq_bf16* x, int64_t M, const int32_t* expert_offsets, int64_t E,
+                         const uint32_t* Wpacked, const wq_bf16* scales, int64_t N, int64_t K, int bits, int group,
+                         wq_bf16* y, void* stream) {
+  t_err[0] = 0;
+  WQ_TRY(check_bits(bits));
+  WQ_TRY(check_group_k(group, K, "K"));
+  WQ_TRY(check_size(M, "M"));
+  WQ_TRY(check_size(N, "N"));
+  if (E < 1 || E > kMaxExperts) return fail(WQ_EINVAL, "E must be in 1..%d (got %lld)", kMaxExperts, (long long)E);
+  if (E * N > kMaxDim) return fail(WQ_EINVAL, "E * N must be below 2^31 (got %lld)", (long long)(E * N));
+  WQ_PTR(x);
+  WQ_PTR(Wpacked);
+  WQ_PTR(scales);
+  WQ_PTR(y);
+  if (expert_offsets == nullptr || (reinterpret_cast<uintptr_t>(expert_offsets) & 3u) != 0)
+    return fail(WQ_EINVAL, "expert_offsets must be a non-NULL, 4-byte aligned device pointer");
+  Ctx c{};
+  WQ_TRY(get_ctx(stream, &c));
+  cudaError_t e = launch_moe(c, x, expert_offsets, E, Wpacked, scales, M, N, K, bits, y);
+  if (e != cudaSuccess) return t_err[0] ? WQ_ECUDA : cuda_fail(e, "wna16_moe_gemm launch");
+  return WQ_OK;
 }
 
 wq_status act_quant_int8(const wq_bf16* x, int64_t M, int64_t K, int8_t* xq, float* sx,

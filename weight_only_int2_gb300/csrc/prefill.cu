@@ -90,12 +90,58 @@ struct PParams {
   const uint8_t* zeros;    // asymmetric groups: zero points [N, G], or null (2^(b-1))
   int64_t M, N, K;
   int G;
-  int row_tiles, tok_tiles;  // ceil(N / 128), ceil(M / TN)
+  int row_tiles, tok_tiles;  // ceil(N / 128), ceil(M / TN) (without offsets)
+  // Mixture of experts: the tokens come sorted by expert, expert e owning
+  // rows [offsets[e], offsets[e+1]) of x and y; its weights are rows
+  // e N .. e N + N - 1 of the stacked packed tensor and scales. Null for a
+  // single dense layer (E = 1).
+  const int32_t* offsets;
+  int E;
   uint16_t* y;       // bf16 [M, N]
   unsigned* status;
 };
 
 using namespace tc;
+
+// A token tile of the concatenated per-expert sequence: its expert, its
+// first token and the end of that expert's tokens. The offsets are clamped
+// into [0, M] and made nondecreasing, so no tile can reach outside x or y.
+struct TokTile {
+  int e;
+  int64_t m0, mend;
+};
+__device__ __forceinline__ int64_t clamped_offset(const PParams& p, int e, int64_t prev) {
+  int64_t v = p.offsets[e];
+  v = v < prev ? prev : v;
+  return v > p.M ? p.M : v;
+}
+template <int TN>
+__device__ __forceinline__ TokTile tok_tile(const PParams& p, int tt) {
+  if (p.offsets == nullptr) return TokTile{0, static_cast<int64_t>(tt) * TN, p.M};
+  int acc = 0;
+  int64_t prev = clamped_offset(p, 0, 0);
+  for (int e = 0; e < p.E; ++e) {
+    const int64_t nxt = clamped_offset(p, e + 1, prev);
+    const int nt = static_cast<int>((nxt - prev + TN - 1) / TN);
+    if (tt < acc + nt) return TokTile{e, prev + static_cast<int64_t>(tt - acc) * TN, nxt};
+    acc += nt;
+    prev = nxt;
+  }
+  return TokTile{p.E - 1, p.M, p.M};  // past the last tile: no tokens
+}
+// Token tiles of the whole sequence (sum over experts of ceil(tokens / TN)).
+template <int TN>
+__device__ __forceinline__ int tok_tiles_total(const PParams& p) {
+  if (p.offsets == nullptr) return p.tok_tiles;
+  int acc = 0;
+  int64_t prev = clamped_offset(p, 0, 0);
+  for (int e = 0; e < p.E; ++e) {
+    const int64_t nxt = clamped_offset(p, e + 1, prev);
+    acc += static_cast<int>((nxt - prev + TN - 1) / TN);
+    prev = nxt;
+  }
+  return acc;
+}
 
 // ---- dequantization: wq_dequant.cuh -----------------------------------------
 
@@ -117,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t full[kNA], done[kNA], pfull[kMaxNP], pempty[kMaxNP], tfull, tempty;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
+  __shared__ int s_tok_tiles;
 
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* base = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -129,7 +176,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // static schedule: tiles blockIdx.x, blockIdx.x + gridDim.x, ...; row
   // tiles vary fastest so that CTAs running together share activation tiles
   const int first = blockIdx.x, step = gridDim.x;
-  const int ntiles = p.row_tiles * p.tok_tiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNA; ++s) {
@@ -143,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&tfull, 1);
     mbar_init(&tempty, kDeqWarps);
     s_abort = 0;
+    s_tok_tiles = tok_tiles_total<TN>(p);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -155,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
+  const int ntiles = p.row_tiles * s_tok_tiles;
 
   if (warp == 0) {
     // ---- activations: stage i of a tile covers k = 64 i .. 64 i + 63; slot
@@ -162,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;  // stages of this CTA's sequence
       for (int t = first; t < ntiles && !s_abort; t += step) {
-        const int m0 = (t / p.row_tiles) * TN;
+        const int m0 = static_cast<int>(tok_tile<TN>(p, t / p.row_tiles).m0);
         for (int i = 0; i < S; ++i, ++it) {
           if (it >= static_cast<uint32_t>(NX)) {
             const uint32_t j = it - NX;
@@ -184,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t gi = 0;  // groups of this CTA's sequence
       for (int t = first; t < ntiles && !s_abort; t += step) {
-        const int n0 = (t % p.row_tiles) * kBM;
+        // rows of the stacked weights: expert e's layer starts at row e N
+        const int n0 = tok_tile<TN>(p, t / p.row_tiles).e * static_cast<int>(p.N) + (t % p.row_tiles) * kBM;
         for (int g = 0; g < G; ++g, ++gi) {
           const uint32_t sl = gi % NP;
           if (gi >= static_cast<uint32_t>(NP) && !mbar_wait_bounded(&pempty[sl], ((gi / NP) - 1) & 1)) {
@@ -256,13 +305,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ng >= G && nt < ntiles) ng -= G, nt += step;
     // the scale bits and (asymmetric groups) the zero point of that group,
     // as scale | zero << 16
+    int s_nt = -1;
+    int64_t s_wrow = 0;  // stacked row of this thread's weight row in tile s_nt (or -1)
     auto load_scale = [&]() -> uint32_t {
       uint32_t v = 0;
       if (nt < ntiles) {
-        const int64_t row = static_cast<int64_t>(nt % p.row_tiles) * kBM + r;
-        if (row < p.N) {
-          v = p.scales[row * G + ng];
-          if (p.zeros != nullptr) v |= static_cast<uint32_t>(p.zeros[row * G + ng]) << 16;
+        if (nt != s_nt) {
+          s_nt = nt;
+          const int64_t row = static_cast<int64_t>(nt % p.row_tiles) * kBM + r;
+          s_wrow = row < p.N ? static_cast<int64_t>(tok_tile<TN>(p, nt / p.row_tiles).e) * p.N + row : -1;
+        }
+        if (s_wrow >= 0) {
+          v = p.scales[s_wrow * G + ng];
+          if (p.zeros != nullptr) v |= static_cast<uint32_t>(p.zeros[s_wrow * G + ng]) << 16;
         }
       }
       ng += 2;
@@ -285,8 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty);
+      const TokTile tk = tok_tile<TN>(p, t / p.row_tiles);
       const int64_t n = static_cast<int64_t>(t % p.row_tiles) * kBM + r;
-      const int64_t m0 = static_cast<int64_t>(t / p.row_tiles) * TN + team * kCols;
+      const int64_t m0 = tk.m0 + team * kCols;
       if (n < p.N) {
         uint16_t* dst = p.y + m0 * p.N + n;
 #pragma unroll
@@ -294,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int64_t m = m0 + 32 * c + j;
-            if (m < p.M) {
+            if (m < tk.mend) {
               const float f = __uint_as_float(v[c][j]);
               dst[static_cast<int64_t>(32 * c + j) * p.N] = float_to_bf16_bits_rn(f);
             }
@@ -402,8 +458,11 @@ cudaError_t plaunch(const Ctx& c, const CUtensorMap& xmap, const CUtensorMap& wm
   PParams q = prm;
   q.row_tiles = static_cast<int>((prm.N + kBM - 1) / kBM);
   q.tok_tiles = static_cast<int>((prm.M + TN - 1) / TN);
-  const int tiles = q.row_tiles * q.tok_tiles;
-  const int grid = tiles < c.sm_count ? tiles : c.sm_count;  // persistent: one CTA per SM
+  // with experts the tiles are known on the device only: at most one
+  // partial token tile per expert beyond ceil(M / TN)
+  const int64_t tiles64 = static_cast<int64_t>(q.row_tiles) * (q.tok_tiles + (prm.offsets ? prm.E : 0));
+  const int tiles = tiles64 < c.sm_count ? static_cast<int>(tiles64) : c.sm_count;
+  const int grid = tiles;  // persistent: one CTA per SM
   prefill_kernel<B, TN><<<grid, kThreads, smem, c.stream>>>(xmap, wmap, q);
   return cudaGetLastError();
 }
@@ -434,9 +493,11 @@ bool prefill_supported(int64_t M, int64_t N, int64_t K, int bits) {
          bits >= 2 && bits <= 8;
 }
 
-cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* packed, const uint16_t* scales,
-                           int64_t M, int64_t N, int64_t K, int bits, uint16_t* y, const uint8_t* zeros) {
-  const int tn = prefill_tile_tokens(M);
+static cudaError_t launch_tc(const Ctx& c, const uint16_t* x, const uint32_t* packed, const uint16_t* scales,
+                             const uint8_t* zeros, const int32_t* offsets, int64_t E, int64_t M, int64_t N, int64_t K,
+                             int bits, uint16_t* y) {
+  // tokens per tile from the tokens per expert (all of them for one layer)
+  const int tn = prefill_tile_tokens((M + E - 1) / E);
   CUtensorMap xmap, wmap;
   if (!make_tmap_bf16_2d_sw128(&xmap, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBK,
                                static_cast<uint32_t>(tn)))
@@ -444,11 +505,14 @@ cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* pack
   const uint64_t words = static_cast<uint64_t>(K) * bits / 32;
   // rows of a power-of-two pitch (2, 4, 8 bits: 32, 64, 128 bytes) would put
   // every row on the same banks; the TMA swizzle of that span spreads them
-  if (!make_tmap_u32_2d(&wmap, packed, words, static_cast<uint64_t>(N), 4u * bits, kBM, packed_swizzle_bytes(bits)))
+  if (!make_tmap_u32_2d(&wmap, packed, words, static_cast<uint64_t>(E * N), 4u * bits, kBM,
+                        packed_swizzle_bytes(bits)))
     return cudaErrorInvalidValue;
   PParams prm{};
   prm.scales = scales;
   prm.zeros = zeros;
+  prm.offsets = offsets;
+  prm.E = static_cast<int>(E);
   prm.M = M;
   prm.N = N;
   prm.K = K;
@@ -456,6 +520,16 @@ cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* pack
   prm.y = y;
   prm.status = c.status;
   return tn == 128 ? plaunch_b<128>(c, bits, xmap, wmap, prm) : plaunch_b<256>(c, bits, xmap, wmap, prm);
+}
+
+cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* packed, const uint16_t* scales,
+                           int64_t M, int64_t N, int64_t K, int bits, uint16_t* y, const uint8_t* zeros) {
+  return launch_tc(c, x, packed, scales, zeros, nullptr, 1, M, N, K, bits, y);
+}
+
+cudaError_t launch_moe(const Ctx& c, const uint16_t* x, const int32_t* offsets, int64_t E, const uint32_t* packed,
+                       const uint16_t* scales, int64_t M, int64_t N, int64_t K, int bits, uint16_t* y) {
+  return launch_tc(c, x, packed, scales, nullptr, offsets, E, M, N, K, bits, y);
 }
 
 }  // namespace wq

@@ -119,6 +119,14 @@ bool prefill_supported(int64_t M, int64_t N, int64_t K, int bits);
 cudaError_t launch_prefill(const Ctx& c, const uint16_t* x, const uint32_t* packed, const uint16_t* scales,
                            int64_t M, int64_t N, int64_t K, int bits, uint16_t* y, const uint8_t* zeros);
 
+// Mixture of experts on the same kernel: tokens sorted by expert, expert e
+// owning rows [offsets[e], offsets[e+1]) of x [M, K] and y [M, N] (offsets: a
+// device array of E + 1 values, clamped into [0, M] by the kernel); its
+// weights are rows e N .. e N + N - 1 of the stacked packed [E N, words] and
+// scales [E N, K/128].
+cudaError_t launch_moe(const Ctx& c, const uint16_t* x, const int32_t* offsets, int64_t E, const uint32_t* packed,
+                       const uint16_t* scales, int64_t M, int64_t N, int64_t K, int bits, uint16_t* y);
+
 // W4A8 on the tensor cores with exact per-group integer accumulation
 // (w4a8tc.cu): xqb holds the per-token int8 codes as bf16 values [M, K] and sx
 // the token scales [M]; writes y [M, N], or with acc != nullptr the group
