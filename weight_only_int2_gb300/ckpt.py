@@ -216,12 +216,12 @@ def to_device(layer: QuantLayer, device="cuda"):
 
     from . import _lib
 
-    s_dev = torch.from_numpy(np.ascontiguousarray(layer.scales).view(np.int16)).view(torch.bfloat16).to(device)
-    z_dev = None if layer.zeros is None else torch.from_numpy(np.ascontiguousarray(layer.zeros)).to(device)
+    s_dev = torch.from_numpy(np.array(layer.scales, dtype=np.uint16, order="C", copy=True).view(np.int16)).view(torch.bfloat16).to(device)
+    z_dev = None if layer.zeros is None else torch.from_numpy(np.array(layer.zeros, dtype=np.uint8, order="C", copy=True)).to(device)
     if layer.packed is not None:
-        p_dev = torch.from_numpy(np.ascontiguousarray(layer.packed)).to(device)
+        p_dev = torch.from_numpy(np.array(layer.packed, dtype=np.int32, order="C", copy=True)).to(device)
     else:
-        c_dev = torch.from_numpy(np.ascontiguousarray(layer.codes)).to(device)
+        c_dev = torch.from_numpy(np.array(layer.codes, dtype=np.uint8, order="C", copy=True)).to(device)
         p_dev, _ = _lib.wna16_repack(c_dev, s_dev, layer.bits)
     return p_dev, s_dev, z_dev
 
