@@ -207,6 +207,9 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
     // (they wait on it, then fence, before their first barrier operation);
     // the peer CTA learns of it through the cluster barrier.
     if (lane == 0) {
+      // the two descriptors are fetched while the barriers are set up
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&wmap)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&smap)) : "memory");
       for (int s = 0; s < NS; ++s) {
         mbar_init(&full[s], 1);
         mbar_init(&empty[s], T);  // the T warps (one per tile) that read a stage

@@ -8,6 +8,7 @@
 
 #include "wq_device.cuh"
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 namespace wq {
@@ -140,10 +141,6 @@ __device__ __forceinline__ void mma16(float (&c)[4], uint32_t a0, uint32_t a1, u
   }
 }
 
-__device__ __forceinline__ uint16_t f32_to_f16_bits_rn(float f) {
-  return __half_as_ushort(__float2half_rn(f));
-}
-
 
 // ---------------------------------------------------------------------------
 // Activation staging. A thread owns slice t (32 consecutive activations) of
@@ -215,12 +212,13 @@ __device__ __forceinline__ void make_fragments(const float (&v)[32], uint32_t (&
     const float xlo = v[sp.lo], xhi = v[sp.hi];
     sum += xlo + xhi;
     sum_o = fmaf(xlo, flo, fmaf(xhi, fhi, sum_o));
+    // one paired round-to-nearest conversion per register (lo in the low half)
     if constexpr (kF16) {
-      frag[q] = static_cast<uint32_t>(f32_to_f16_bits_rn(xlo * flo * inv)) |
-                (static_cast<uint32_t>(f32_to_f16_bits_rn(xhi * fhi * inv)) << 16);
+      const __half2 h = __floats2half2_rn(xlo * flo * inv, xhi * fhi * inv);
+      frag[q] = *reinterpret_cast<const uint32_t*>(&h);
     } else {
-      frag[q] = static_cast<uint32_t>(float_to_bf16_bits_rn(xlo)) |
-                (static_cast<uint32_t>(float_to_bf16_bits_rn(xhi)) << 16);
+      const __nv_bfloat162 h = __floats2bfloat162_rn(xlo, xhi);
+      frag[q] = *reinterpret_cast<const uint32_t*>(&h);
     }
   }
   sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
