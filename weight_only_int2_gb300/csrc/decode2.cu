@@ -606,15 +606,27 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
         record_status(p.status, kStatusTimeout);
         s_abort = 1;
       }
-      if (ready) {
-        for (int e = threadIdx.x; e < half_rows * kTok; e += kCWarps * 32) {
-          const int rr = e % half_rows, tok = e / half_rows;
+      // (a thread takes four token columns of one row: 16-byte reads of
+      // consecutive words, no bank conflicts; the quads past M are skipped)
+      if (kMode != 2 && ready) {
+        const int mq = (static_cast<int>(p.M) + 3) / 4;  // token quads holding real tokens
+        for (int e = threadIdx.x; e < half_rows * mq; e += kCWarps * 32) {
+          const int rr = e / mq, c4 = e % mq;
           const int rl = static_cast<int>(q) * half_rows + rr;
           const int64_t row = rc + rl;
-          if (kMode != 2 && tok < p.M && rl < H && row < r1) {  // tile rows past H are not the chunk's
-            float v = part[rl * kTok + tok] + inbox[rr * kTok + tok];
-            if constexpr (kQuant) v *= s_sx[tok];
-            p.y[tok * p.N + row] = float_to_bf16_bits_rn(v);
+          if (rl < H && row < r1) {  // tile rows past H are not the chunk's
+            const float4 a = *reinterpret_cast<const float4*>(part + rl * kTok + 4 * c4);
+            const float4 b = *reinterpret_cast<const float4*>(inbox + rr * kTok + 4 * c4);
+            const float v[4] = {a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int tok = 4 * c4 + i;
+              if (tok < p.M) {
+                float vi = v[i];
+                if constexpr (kQuant) vi *= s_sx[tok];
+                p.y[tok * p.N + row] = float_to_bf16_bits_rn(vi);
+              }
+            }
           }
         }
       }
