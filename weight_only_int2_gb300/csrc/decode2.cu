@@ -630,14 +630,16 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
           }
         }
       }
-      consumer_sync();  // our inbox has been read: the peer may fill it again
-      if (threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(dbar), peer));
+      // our inbox has been read: the peer may fill it again (after the last
+      // chunk nothing more is sent, and each CTA leaves on its own: every
+      // access of one CTA to the other's shared memory, the peer's sums and
+      // its arrival on "ready", has completed once that CTA's wait on
+      // "ready" returned)
+      if (k + 1 < nck) {
+        consumer_sync();
+        if (threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(dbar), peer));
+      }
     }
-    // The pair leaves together: waiting for the peer's last arrival (measured:
-    // letting each CTA leave as soon as its rows are written is slower when
-    // the next kernel launches programmatically).
-    if (nck >= 1 && !mbar_wait_cluster_bounded(dbar, (nck - 1) & 1, lim) && threadIdx.x == 0)
-      record_status(p.status, kStatusTimeout);
   }
   __syncthreads();
 }
