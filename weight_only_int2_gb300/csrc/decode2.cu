@@ -25,8 +25,10 @@
 //    fp32 accumulators with the group scale applied per group.
 //  * Per chunk: the warps of a tile reduce in shared memory in a fixed order;
 //    each CTA pushes its sums of the rows its peer finalises into the peer's
-//    inbox (remote 16-byte stores) and arrives on the peer's "ready" barrier;
-//    each CTA then writes half the rows. A "consumed" arrival frees the inbox.
+//    inbox with remote asynchronous 16-byte stores that count their bytes on
+//    the peer's "ready" barrier; each CTA then writes half the rows. A
+//    "consumed" arrival frees the inbox for the next chunk; after the last
+//    chunk each CTA leaves on its own.
 //  * Programmatic dependent launch: the kernel lets the next one in the
 //    stream launch at once; the producer streams weights and scales (never
 //    written by these kernels) right away, the consumers wait for the
@@ -586,20 +588,22 @@ __global__ void __launch_bounds__(kThreads2, 1) decode2_kernel(const __grid_cons
       // the peer's barriers exist (it arrived on the cluster barrier after
       // initialising them) before anything of ours reaches its memory
       if (k == 0) cluster_wait();
-      // push our sums of the rows the peer finalises into its inbox (remote
-      // 16-byte stores, no waiting), then tell it they are there
+      // push our sums of the rows the peer finalises into its inbox: remote
+      // 16-byte asynchronous stores, each counting its bytes on the peer's
+      // "ready" barrier, which completes once all have landed (and its own
+      // CTA has announced the byte count of the chunk)
       const int half_rows = T * (kTileRows / 2);
       {
-        const uint32_t pin = map_peer(smem_u32(inbox), peer);
         const int nvec = half_rows * (kTok / 4);
+        if (threadIdx.x == 0) mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(nvec) * 16u);
+        const uint32_t pin = map_peer(smem_u32(inbox), peer);
+        const uint32_t prbar = map_peer(smem_u32(rbar), peer);
         for (int e = threadIdx.x; e < nvec; e += kCWarps * 32) {
           const int rr = e / (kTok / 4), c4 = e % (kTok / 4);
           const float4 v = *reinterpret_cast<const float4*>(part + (static_cast<int>(peer) * half_rows + rr) * kTok + 4 * c4);
-          st_peer_v4(pin + 16u * static_cast<uint32_t>(rr * (kTok / 4) + c4), v);
+          st_async_peer_v4(pin + 16u * static_cast<uint32_t>(rr * (kTok / 4) + c4), v, prbar);
         }
       }
-      consumer_sync();
-      if (threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(rbar), peer));
       // the peer's sums of our rows are in our inbox: combine, write y
       const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait_cluster_bounded(rbar, k & 1, lim));
       if (!ready && threadIdx.x == 0) {

@@ -58,9 +58,14 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
-__device__ __forceinline__ void st_peer_v4(uint32_t cluster_addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x), "f"(v.y),
-               "f"(v.z), "f"(v.w)
+// Remote 16-byte store into the peer's shared memory that counts its bytes
+// on the peer's mbarrier (complete_tx): the peer's wait on that barrier
+// returns once every such store has landed, with no release/arrive round
+// trip on the sending side.
+__device__ __forceinline__ void st_async_peer_v4(uint32_t cluster_addr, float4 v, uint32_t cluster_mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   cluster_addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(cluster_mbar)
                : "memory");
 }
 // Programmatic dependent launch: let the next kernel of the stream start
