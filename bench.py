@@ -51,7 +51,7 @@ def _peaks():
 
 def _kernel_hash():
     h = hashlib.sha256()
-    for f in ("decode2.cu", "wq_unpack.cuh", "wq_device.cuh"):
+    for f in ("decode2.cu", "wq_unpack.cuh", "wq_device.cuh", "wq_cluster.cuh"):
         h.update(open(os.path.join(ROOT, "weight_only_int2_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
