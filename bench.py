@@ -358,11 +358,56 @@ def _rand_layer(wq, torch, N, K, bits, gen):
     return packed, s
 
 
+L2_BYTES = 129 * 2**20
+ROTATE_BYTES = 3 * L2_BYTES  # a timed rotation reads at least this much distinct data
+
+
+def _sms(torch) -> int:
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _copies(nbytes: float) -> int:
+    """Distinct copies of an input of nbytes that a timed rotation cycles
+    through, so that each call reads its data from HBM, not from L2."""
+    return max(1, int(-(-ROTATE_BYTES // max(1, int(nbytes)))))
+
+
+def _rotation_ms(torch, stream, fns, reps):
+    """Average device time of one call, over a CUDA graph that makes the calls
+    fns[0..R-1] in turn (each on its own copy of the data), replayed reps
+    times."""
+    def step():
+        for f in fns:
+            f()
+    return _graph_ms(torch, stream, step, reps) / len(fns)
+
+
+def _mma_peaks(wq, torch, stream):
+    """The warp-level tensor-core peaks (mma.sync) of this GPU, int8
+    (m16n8k32, int32 accumulate) and bf16 (m16n8k16, fp32 accumulate), from
+    the library's probe; each launch's checksums are verified exactly."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    blocks, iters = 4 * sms, 20000
+    res = {}
+    for kind, k, name in ((0, 32, "int8_mma_sync_tops"), (1, 16, "bf16_mma_sync_tflops")):
+        out = torch.empty(blocks * 256, dtype=torch.int32, device="cuda")
+        ms = _event_ms(torch, stream, lambda: wq.debug_mma_peak(kind, iters, blocks, out), 5)
+        if not bool((out == 8 * 4 * k * iters).all()):
+            raise RuntimeError(f"mma.sync probe kind {kind}: wrong checksums")
+        ops = blocks * 8 * 8 * iters * 2 * 16 * 8 * k
+        res[name] = round(ops / (ms * 1e-3) / 1e12, 1)
+    return res
+
+
 def _time_extras(wq, torch, stream, only=None):
     """The other rows of the scope table, each against its roofline: prefill
     sweep, the decode configuration's M = 64 cases, W4A8, the 8-bit lm_head,
     the embedding gather and the 64-layer mixed-bit stack (timed as one CUDA
-    graph). `only` names one of them to time alone (profiling)."""
+    graph), the mma.sync peaks and the cost of the no-allocation entry point.
+    Every row reads its weights from HBM: a row whose data fits L2 cycles
+    through distinct copies of at least 3x L2; the others are larger than L2.
+    Calls are timed in groups of at least 20. `only` names one row to time
+    alone (profiling)."""
 
     def want(name):
         return only is None or only == name
@@ -390,7 +435,7 @@ def _time_extras(wq, torch, stream, only=None):
             for M in (2048, 8192):
                 x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
                 y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-                ms = _event_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, N, K, bits, y=y), 3)
+                ms = _event_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, N, K, bits, y=y), 20)
                 rows.append(dict(bits=bits, M=M, **tfl(2.0 * M * N * K, ms)))
             del packed, s
         out["prefill"] = rows
@@ -401,30 +446,41 @@ def _time_extras(wq, torch, stream, only=None):
         rows = []
         for bits in (5, 6, 7):
             for Nd in (5120, 17408):
-                packed, s = _rand_layer(wq, torch, Nd, K, bits, gen)
+                nb = Nd * K * bits / 8
+                layers = [_rand_layer(wq, torch, Nd, K, bits, gen) for _ in range(_copies(nb))]
                 x = torch.randn(64, K, device="cuda", generator=gen).to(torch.bfloat16)
                 y = torch.empty(64, Nd, dtype=torch.bfloat16, device="cuda")
                 ws = torch.zeros(max(1, wq.wna16_workspace_bytes(64, Nd, K, bits)), dtype=torch.uint8, device="cuda")
-                ms = _graph_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, Nd, K, bits, y=y, ws=ws), 50)
-                rows.append(dict(bits=bits, N=Nd, M=64, **gbs(Nd * K * bits / 8, ms)))
-                del packed, s
+                fns = [lambda pk=pk, sc=sc: wq.wna16_gemm(x, pk, sc, Nd, K, bits, y=y, ws=ws) for pk, sc in layers]
+                ms = _rotation_ms(torch, stream, fns, 20)
+                rows.append(dict(bits=bits, N=Nd, M=64, copies=len(layers), **gbs(nb, ms)))
+                del layers
         out["decode_m64"] = rows
 
     if want("w4a8"):
-        # W4A8 (int8 activations quantized per token inside the call)
-        packed, s = _rand_layer(wq, torch, N, K, 4, gen)
+        # W4A8 (int8 activations quantized per token inside the call), against
+        # the measured bf16 peak (the exact path multiplies on the bf16 tensor
+        # cores) and beside it the measured int8 mma.sync peak
+        peaks = _mma_peaks(wq, torch, stream)
+        out["mma_sync_peaks"] = peaks
+        nb = N * K * 4 / 8
+        layers = [_rand_layer(wq, torch, N, K, 4, gen) for _ in range(_copies(nb))]
+        packed, s = layers[0]
         rows = []
         for M in (1, 512, 8192):
             x = torch.randn(M, K, device="cuda", generator=gen).to(torch.bfloat16)
             y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
             if M == 1:
-                ms = _graph_ms(torch, stream, lambda: wq.w4a8_gemm(x, packed, s, N, K, y=y), 200)
-                rows.append(dict(M=M, **gbs(N * K * 4 / 8, ms)))
+                fns = [lambda pk=pk, sc=sc: wq.w4a8_gemm(x, pk, sc, N, K, y=y) for pk, sc in layers]
+                ms = _rotation_ms(torch, stream, fns, 20)
+                rows.append(dict(M=M, copies=len(layers), **gbs(nb, ms)))
             else:
-                ms = _event_ms(torch, stream, lambda: wq.w4a8_gemm(x, packed, s, N, K, y=y), 3)
-                rows.append(dict(M=M, **tfl(2.0 * M * N * K, ms)))
+                ms = _event_ms(torch, stream, lambda: wq.w4a8_gemm(x, packed, s, N, K, y=y), 20)
+                r = dict(M=M, **tfl(2.0 * M * N * K, ms))
+                r["frac_int8_mma_sync"] = round(r["TFLOPS"] / peaks["int8_mma_sync_tops"], 4)
+                rows.append(r)
         out["w4a8"] = rows
-        del packed, s
+        del layers, packed, s
 
     if want("lm_head") or want("gather"):
         # lm_head: 8-bit, N = 248320 (1.27 GB packed), and the gather from the same table
@@ -439,15 +495,27 @@ def _time_extras(wq, torch, stream, only=None):
                     ms = _graph_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, V, K, 8, y=y), 20)
                     rows.append(dict(M=M, **gbs(V * K, ms)))
                 else:
-                    ms = _event_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, V, K, 8, y=y), 3)
+                    ms = _event_ms(torch, stream, lambda: wq.wna16_gemm(x, packed, s, V, K, 8, y=y), 20)
                     rows.append(dict(M=M, **tfl(2.0 * M * V * K, ms)))
             out["lm_head"] = rows
         if want("gather"):
+            # distinct id sets and output buffers in turn (at least 3x L2 of
+            # rows read and written), so that rows and outputs go through HBM
             T = 4096
-            ids = torch.randint(0, V, (T,), dtype=torch.int32, device="cuda", generator=gen)
-            ms = _graph_ms(torch, stream, lambda: wq.qembed_gather(ids, packed, s, V, K, 8), 100)
             moved = T * (K + 2 * K // 128 + 2 * K + 4)  # packed row + scales in, bf16 row out, id
-            out["gather"] = dict(T=T, bytes_moved=moved, **gbs(moved, ms))
+            R = _copies(moved)
+            sets = [(torch.randint(0, V, (T,), dtype=torch.int32, device="cuda", generator=gen),
+                     torch.empty(T, K, dtype=torch.bfloat16, device="cuda")) for _ in range(R)]
+            fns = [lambda ids=ids, o=o: wq.qembed_gather(ids, packed, s, V, K, 8, out=o) for ids, o in sets]
+            ms = _rotation_ms(torch, stream, fns, 20)
+            # DRAM sees the reads within the launch; the written rows land in
+            # L2 and reach HBM later (an ncu dram__bytes check)
+            read = T * (K + 2 * K // 128 + 4)
+            g = gbs(moved, ms)
+            g["read_GBps"] = round(read / (ms * 1e-3) / 1e9, 1)
+            g["read_frac"] = round(g["read_GBps"] / hbm, 4)
+            out["gather"] = dict(T=T, bytes_moved=moved, bytes_read=read, id_sets=R, **g)
+            del sets
         del packed, s
 
     if want("stack"):
@@ -467,12 +535,32 @@ def _time_extras(wq, torch, stream, only=None):
                 for li, (b, pk, sc) in enumerate(layers):
                     wq.wna16_gemm(x, pk, sc, N, K, b, y=ys[li & 1])
 
-            ms = _graph_ms(torch, stream, stack, 3 if M > 1 else 10)
+            ms = _graph_ms(torch, stream, stack, 20)
             if M == 1:
                 rows.append(dict(M=M, layers=64, packed_bytes=int(stack_bytes), **gbs(stack_bytes, ms)))
             else:
                 rows.append(dict(M=M, layers=64, **tfl(2.0 * M * N * K * 64, ms)))
         out["stack"] = rows
+        del layers
+
+    if want("noalloc"):
+        # the no-allocation entry point against the workspace one on a
+        # split-K shape (16 tokens, K = 14336: the pair kernel's K half does
+        # not fit): the difference is the scratch clear it queues per call
+        Mn, Nn, Kn, bn = 16, 17408, 14336, 6
+        nb = Nn * Kn * bn / 8
+        layers = [_rand_layer(wq, torch, Nn, Kn, bn, gen) for _ in range(_copies(nb))]
+        x = torch.randn(Mn, Kn, device="cuda", generator=gen).to(torch.bfloat16)
+        y = torch.empty(Mn, Nn, dtype=torch.bfloat16, device="cuda")
+        ws = torch.zeros(max(1, wq.wna16_workspace_bytes(Mn, Nn, Kn, bn)), dtype=torch.uint8, device="cuda")
+        f_ws = [lambda pk=pk, sc=sc: wq.wna16_gemm(x, pk, sc, Nn, Kn, bn, y=y, ws=ws) for pk, sc in layers]
+        f_na = [lambda pk=pk, sc=sc: wq.wna16_gemm_noalloc(x, pk, sc, Nn, Kn, bn, y=y) for pk, sc in layers]
+        ms_ws = _rotation_ms(torch, stream, f_ws, 20)
+        ms_na = _rotation_ms(torch, stream, f_na, 20)
+        out["noalloc"] = dict(M=Mn, N=Nn, K=Kn, bits=bn, route=wq.debug_route(Mn, Nn, Kn, bn, _sms(torch)),
+                              scratch_bytes=wq.wna16_workspace_bytes(Mn, Nn, Kn, bn),
+                              ms_workspace=round(ms_ws, 4), ms_noalloc=round(ms_na, 4),
+                              copies=len(layers))
         del layers
     torch.cuda.empty_cache()
     return out
@@ -593,7 +681,7 @@ def main():
                     help="skip the other rows (prefill, W4A8, lm_head, gather, stack)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--only", choices=["prefill", "decode_m64", "w4a8", "lm_head", "gather", "stack"],
+    ap.add_argument("--only", choices=["prefill", "decode_m64", "w4a8", "lm_head", "gather", "stack", "noalloc"],
                     default=None, help="time one group of the other rows alone, without the decode sweep")
     ap.add_argument("--prefill-case", type=str, default=None,
                     help="time one prefill shape 'bits,M' (N=17408, K=5120) alone (profiling)")

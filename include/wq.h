@@ -262,6 +262,18 @@ wq_status wq_debug_route(int64_t M, int64_t N, int64_t K, int bits, int kind, in
 wq_status wq_debug_unpack(const uint32_t* packed, int64_t N, int64_t K, int bits,
                           uint8_t* codes, void* stream);
 
+/* Throughput probe of the warp-level tensor-core instruction (mma.sync) in
+ * the two forms the W4A8 discussion weighs [W4A8 "Under the hood": int8
+ * products accumulated in int32, against bf16]: kind 0 runs m16n8k32
+ * s8 x s8 -> s32, kind 1 m16n8k16 bf16 x bf16 -> f32. `blocks` CTAs of 8
+ * warps each run 8 independent chains of `iters` instructions on all-ones
+ * operands and write one int32 checksum per thread to out [blocks * 256]
+ * (device memory, caller-owned), which must equal 8 * 4 * K * iters with
+ * K = 32 (kind 0) or 16 (kind 1). The caller times the launch on `stream`:
+ * operations = blocks * 8 * 8 * iters * 2*16*8*K. WQ_EINVAL for kind not 0/1,
+ * iters outside 1..1000000, blocks outside 1..65535 or a NULL out. */
+wq_status wq_debug_mma_peak(int kind, int64_t iters, int blocks, int32_t* out, void* stream);
+
 /* The exact per-group integer accumulators of the W4A8 main loop [W4A8]:
  *   acc[m, n, g] = sum_{k in group g} xq[m, k] * (q[n, k] - 8),
  * with xq = act_quant_int8(x), computed by the kernel that w4a8_gemm launches

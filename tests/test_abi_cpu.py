@@ -104,6 +104,13 @@ def test_bad_arguments_rejected_before_any_cuda_call(lib, fake):
     assert b"aligned" in lib.wq_last_error()
     # M = 0
     assert lib.wna16_gemm(fake, 0, fake, fake, 8, 128, 6, 128, fake, None, 0, None) == 1
+    # the mma.sync probe: kind, iteration and block bounds, NULL output
+    assert lib.wq_debug_mma_peak(2, 10, 1, fake, None) == 1
+    assert lib.wq_debug_mma_peak(0, 0, 1, fake, None) == 1
+    assert lib.wq_debug_mma_peak(1, 1000001, 1, fake, None) == 1
+    assert lib.wq_debug_mma_peak(0, 10, 0, fake, None) == 1
+    assert lib.wq_debug_mma_peak(0, 10, 1, None, None) == 1
+    assert b"wq_debug_mma_peak" in lib.wq_last_error()
     # workspace too small for a split-K decode shape
     assert lib.wna16_workspace_bytes(1, 5120, 2560, 6) > 16  # else the call below would launch
     assert lib.wna16_gemm(fake, 1, fake, fake, 5120, 2560, 6, 128, fake, fake, 16, None) == 1

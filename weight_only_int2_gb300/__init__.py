@@ -11,6 +11,7 @@ from ._lib import (  # noqa: F401
     check_status,
     ROUTES,
     debug_decode_plan,
+    debug_mma_peak,
     debug_route,
     debug_unpack,
     debug_w4a8_group_acc,

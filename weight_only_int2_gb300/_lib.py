@@ -51,6 +51,7 @@ SIGNATURES = {
     "wq_debug_w4a8_group_acc": (_c_int, [_c_ptr, _c_i64, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_ptr, _c_ptr,
                                          _c_size, _c_ptr]),
     "wq_debug_noalloc_scratch": (_c_int, [_c_ptr, _c_size, _c_int, _c_ptr]),
+    "wq_debug_mma_peak": (_c_int, [_c_int, _c_i64, _c_int, _c_ptr, _c_ptr]),
     "wq_debug_decode_wait_fault": (_c_int, [_c_i64, ctypes.c_uint64]),
     "wq_check_status": (_c_int, []),
     "wq_last_error": (ctypes.c_char_p, []),
@@ -364,6 +365,17 @@ def debug_unpack(packed: torch.Tensor, N: int, K: int, bits: int) -> torch.Tenso
     codes = torch.empty((N, K), dtype=torch.uint8, device=packed.device)
     _check(load().wq_debug_unpack(_ptr(packed), N, K, bits, _ptr(codes), _stream()), "wq_debug_unpack")
     return codes
+
+
+def debug_mma_peak(kind: int, iters: int, blocks: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Launches the mma.sync throughput probe (kind 0: int8 m16n8k32, kind 1:
+    bf16 m16n8k16) on the current stream; returns the per-thread checksums
+    [blocks * 256] int32 (each 8 * 4 * K * iters)."""
+    if out is None:
+        out = torch.empty(blocks * 256, dtype=torch.int32, device="cuda")
+    _need(out, "out", torch.int32, (blocks * 256,))
+    _check(load().wq_debug_mma_peak(kind, iters, blocks, _ptr(out), _stream()), "wq_debug_mma_peak")
+    return out
 
 
 def debug_w4a8_group_acc(x: torch.Tensor, packed4: torch.Tensor, scales: torch.Tensor, N: int, K: int,
