@@ -21,10 +21,11 @@
 // Warp roles:
 //   warp 0      TMA producer for the activation tile [TN x 64] (128-byte
 //               swizzle, zero fill past M) of each stage.
-//   warp 1      allocates tensor memory; one thread issues, per stage, one
-//               barrier wait, 4 MMAs of K = 16 (A from tensor memory, B from
-//               shared memory) and one commit; each finished tile is
-//               committed to the accumulator's "full" barrier.
+//   warp 1      allocates tensor memory; one thread issues, per group (two
+//               stages), the stages' barrier waits, one fence, 8 MMAs of
+//               K = 16 (A from tensor memory, B from shared memory) and one
+//               commit, which releases both stages' slots; each finished
+//               tile is committed to the accumulator's "full" barrier.
 //   warp 2      TMA producer for the packed weights, one group [128 rows x
 //               16*b bytes] per load.
 //   warps 3-18  four teams of 4 warps; team j takes every fourth stage. A
@@ -49,6 +50,12 @@ constexpr int kBK = 64;      // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kNA = 8;       // A stages in tensor memory
 constexpr int kACol = 256;   // A ring: TMEM columns [256, 512), 32 per stage
 constexpr int kTmemCols = 512;
+// Stages per wait, fence and commit of the MMA thread: that thread's
+// synchronisation per stage (~0.1 us) rivals the tensor time of a stage of
+// four 128 x 256 x 16 MMAs (~0.26 us), so it takes the two stages of a group
+// together (measured: 0.79 of the bf16 peak at M = 8192 against 0.71 per
+// stage; four stages per commit starve the A ring at 0.54).
+constexpr int kSPC = 2;
 constexpr int kMaxNX = 6;    // activation stages in shared memory (upper bound)
 constexpr int kMaxNP = 4;    // packed-weight slots, one group each (upper bound)
 constexpr int kTeamWarps = 4;                  // one team: 128 rows x 64 codes
@@ -157,10 +164,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   // full[j]: stage (j mod kNA) has its activation bytes and its A tile
   //          (arrivals: the activation producer's expect-tx + one team);
-  // done[j]: that stage's MMAs completed (one commit), which frees its A slot
-  //          and, kNX stages later in the sequence, its activation slot;
+  // done[p]: the MMAs of stage pair (p mod kNA/2) completed (one commit per
+  //          pair: the MMA thread takes two stages per wait, fence and
+  //          commit), which frees the pair's two A slots and, kNX stages
+  //          later in the sequence, their activation slots;
   // pfull/pempty: packed-weight slots; tfull/tempty: the accumulator.
-  __shared__ __align__(8) uint64_t full[kNA], done[kNA], pfull[kMaxNP], pempty[kMaxNP], tfull, tempty;
+  constexpr int kND = kNA / kSPC;  // commit barriers
+  __shared__ __align__(8) uint64_t full[kNA], done[kND], pfull[kMaxNP], pempty[kMaxNP], tfull, tempty;
+  // the commit barrier that releases stage j of the sequence, and its phase
+  auto pair_bar = [&](uint32_t j) -> uint64_t* { return &done[(j / kSPC) % kND]; };
+  auto pair_phase = [](uint32_t j) -> uint32_t { return ((j / kSPC) / kND) & 1u; };
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
   __shared__ int s_tok_tiles;
@@ -178,10 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int first = blockIdx.x, step = gridDim.x;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNA; ++s) {
-      mbar_init(&full[s], kTeamWarps + 1);
-      mbar_init(&done[s], 1);
-    }
+    for (int s = 0; s < kNA; ++s) mbar_init(&full[s], kTeamWarps + 1);
+    for (int s = 0; s < kND; ++s) mbar_init(&done[s], 1);
     for (int s = 0; s < NP; ++s) {
       mbar_init(&pfull[s], 1);
       mbar_init(&pempty[s], 2 * kTeamWarps);  // the two teams that share a group
@@ -214,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < S; ++i, ++it) {
           if (it >= static_cast<uint32_t>(NX)) {
             const uint32_t j = it - NX;
-            if (!mbar_wait_bounded(&done[j % kNA], (j / kNA) & 1)) {
+            if (!mbar_wait_bounded(pair_bar(j), pair_phase(j))) {
               record_status(p.status, kStatusTimeout);
               s_abort = 1;
               break;
@@ -261,21 +272,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         bool ok = true;
-        for (int i = 0; i < S; ++i, ++it) {
-          const uint32_t a = it % kNA;
-          if (s_abort || !mbar_wait_bounded(&full[a], (it / kNA) & 1)) {
+        // kSPC = 2 stages (one group) per wait, fence and commit; a tile
+        // has an even number of stages, so pairs never straddle tiles
+        for (int i = 0; i < S; i += kSPC, it += kSPC) {
+          bool got = !s_abort;
+#pragma unroll
+          for (int hh = 0; hh < kSPC; ++hh)
+            if (got) got = mbar_wait_bounded(&full[(it + hh) % kNA], ((it + hh) / kNA) & 1);
+          if (!got) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t bb = smem_u32(xs + (it % NX) * L::kXStage);
-          const uint32_t aa = tmem + kACol + a * (kBK / 2);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // K = 16: 8 more A columns, 32 more bytes along the swizzled B rows
-            umma_bf16_ta(tmem, aa + 8 * kk, sw128_desc(bb + 32 * kk), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int hh = 0; hh < kSPC; ++hh) {
+            const uint32_t bb = smem_u32(xs + ((it + hh) % NX) * L::kXStage);
+            const uint32_t aa = tmem + kACol + ((it + hh) % kNA) * (kBK / 2);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              // K = 16: 8 more A columns, 32 more bytes along the swizzled B rows
+              umma_bf16_ta(tmem, aa + 8 * kk, sw128_desc(bb + 32 * kk), idesc, (i + hh > 0 || kk > 0) ? 1u : 0u);
+            }
           }
-          umma_commit(&done[a]);  // fires when this stage's MMAs complete
+          umma_commit(pair_bar(it));  // fires when the pair's MMAs complete
         }
         umma_commit(&tfull);  // fires once the tile's MMAs have completed
         if (!ok) {
@@ -383,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // and the .sync.aligned tcgen05 instructions)
         bool go = !s_abort;
         if (go) go = mbar_wait_bounded(&pfull[pslot], (gi / NP) & 1);
-        if (go && it >= static_cast<uint32_t>(kNA)) go = mbar_wait_bounded(&done[a], ((it / kNA) - 1) & 1);
+        if (go && it >= static_cast<uint32_t>(kNA)) go = mbar_wait_bounded(pair_bar(it - kNA), pair_phase(it - kNA));
         if (!__all_sync(0xFFFFFFFFu, go)) {
           if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
           s_abort = 1;
