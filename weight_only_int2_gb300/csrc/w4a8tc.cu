@@ -23,9 +23,10 @@
 // Warp roles:
 //   warp 0      TMA producer for the activation codes [TN x 64] (bf16,
 //               128-byte swizzle, zero fill past M) of each stage.
-//   warp 1      allocates tensor memory; one thread issues, per stage, one
-//               barrier wait, 4 MMAs of K = 16 and one commit, and commits
-//               each finished group to its accumulator's "full" barrier.
+//   warp 1      allocates tensor memory; one thread issues, per group, the
+//               waits for its accumulator and its two stages, one fence, 8
+//               MMAs of K = 16 and one commit (the group's barrier: its
+//               accumulator is complete and its slots are free).
 //   warp 2      TMA producer for the packed 4-bit weights, one group
 //               [128 rows x 64 bytes] per load.
 //   warps 3-18  four teams of 4 warps. Team j writes the A operand of the
@@ -53,7 +54,8 @@ using namespace tc;
 
 constexpr int kBM = 128;        // weight rows per tile (MMA M)
 constexpr int kBK = 64;         // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kNB = 8;          // stage barriers (full/done), indexed by stage mod 8
+constexpr int kNB = 8;          // stage barriers (full), indexed by stage mod 8
+constexpr int kNG = 8;          // group barriers (gdone), indexed by group mod 8
 constexpr int kTmemCols = 512;
 constexpr int kMaxNX = 8;       // activation stages in shared memory (<= kNB)
 constexpr int kNP = 4;          // packed-weight slots, one group each (even)
@@ -126,11 +128,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   // full[j]: stage (j mod kNB) has its activation bytes and its A operand
   //          (arrivals: the activation producer's expect-tx + one team);
-  // done[j]: that stage's MMAs completed (one commit): frees its A slot and,
-  //          NX stages later in the sequence, its activation slot;
+  // gdone[g]: the MMAs of group (g mod kNG) completed (one commit per group,
+  //          after both its stages): the group's accumulator is complete, its
+  //          two A slots are free and, NX stages later in the sequence, its
+  //          activation slots;
   // pfull/pempty: packed-weight slots;
-  // accf[b]/acce[b]: group accumulator b complete / read out.
-  __shared__ __align__(8) uint64_t full[kNB], done[kNB], pfull[kNP], pempty[kNP], accf[2], acce[2];
+  // acce[b]: group accumulator b read out.
+  __shared__ __align__(8) uint64_t full[kNB], gdone[kNG], pfull[kNP], pempty[kNP], acce[2];
+  // the group barrier that releases stage j of the sequence, and its phase
+  auto gbar = [&](uint32_t j) -> uint64_t* { return &gdone[(j >> 1) % kNG]; };
+  auto gphase = [](uint32_t j) -> uint32_t { return ((j >> 1) / kNG) & 1u; };
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
 
@@ -150,18 +157,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t total_groups = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(G);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNB; ++s) {
-      mbar_init(&full[s], kTeamWarps + 1);
-      mbar_init(&done[s], 1);
-    }
+    for (int s = 0; s < kNB; ++s) mbar_init(&full[s], kTeamWarps + 1);
+    for (int s = 0; s < kNG; ++s) mbar_init(&gdone[s], 1);
     for (int s = 0; s < kNP; ++s) {
       mbar_init(&pfull[s], 1);
       mbar_init(&pempty[s], 2 * kTeamWarps);  // the two teams that share a group
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], kDeqWarps);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(&acce[b], kDeqWarps);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < S; ++i, ++it) {
           if (it >= static_cast<uint32_t>(NX)) {
             const uint32_t j = it - NX;
-            if (!mbar_wait_backoff<256>(&done[j % kNB], (j / kNB) & 1)) {
+            if (!mbar_wait_backoff<256>(gbar(j), gphase(j))) {
               record_status(p.status, kStatusTimeout);
               s_abort = 1;
               break;
@@ -232,22 +234,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
+        // both stages of the group, then one fence, 8 MMAs and one commit
+        if (s_abort || !mbar_wait_bounded(&full[it % kNB], (it / kNB) & 1) ||
+            !mbar_wait_bounded(&full[(it + 1) % kNB], ((it + 1) / kNB) & 1)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        for (int h = 0; h < 2; ++h, ++it) {
-          if (s_abort || !mbar_wait_bounded(&full[it % kNB], (it / kNB) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t bb = smem_u32(xs + (it % NX) * L::kXStage);
-          const uint32_t aa = tmem + L::kACol + (it % NA) * (kBK / 2);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t bb = smem_u32(xs + ((it + h) % NX) * L::kXStage);
+          const uint32_t aa = tmem + L::kACol + ((it + h) % NA) * (kBK / 2);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             umma_bf16_ta(tmem + b * TN, aa + 8 * kk, sw128_desc(bb + 32 * kk), idesc, (h > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&done[it % kNB]);  // fires when this stage's MMAs complete
         }
-        if (!ok) break;
-        umma_commit(&accf[b]);  // the group's accumulator is complete
+        umma_commit(gbar(it));  // fires when the group's MMAs complete
+        it += 2;
       }
       if (!ok) {
         record_status(p.status, kStatusTimeout);
@@ -274,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t it = 2 * gi + h, a = it % NA, pslot = gi % kNP;
       bool go = !s_abort;
       if (go) go = mbar_wait_backoff<32>(&pfull[pslot], (gi / kNP) & 1);
-      if (go && it >= static_cast<uint32_t>(NA)) go = mbar_wait_backoff<32>(&done[(it - NA) % kNB], ((it - NA) / kNB) & 1);
+      if (go && it >= static_cast<uint32_t>(NA)) go = mbar_wait_backoff<32>(gbar(it - NA), gphase(it - NA));
       if (!__all_sync(0xFFFFFFFFu, go)) {
         if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
         s_abort = 1;
@@ -321,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 1. read out group gi: the MMAs of group gi + 2 wait for this buffer,
       //    so it comes first; the A operand is needed one group later
       const uint32_t b = gi & 1u;
-      if (failed || !__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_backoff<32>(&accf[b], (gi >> 1) & 1))) {
+      if (failed || !__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_backoff<32>(&gdone[gi % kNG], (gi / kNG) & 1))) {
         if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
         s_abort = 1;
         break;
