@@ -196,13 +196,63 @@ static bool ensure_encode() {
   return g_encode != nullptr;
 }
 
+// A descriptor is a pure function of its encoding arguments (the address
+// included), so an encoded one can be reused whenever the same arguments
+// recur, whatever happened to the memory in between. A call's descriptors are
+// looked up in a small table before the driver encodes them: the per-call
+// host work of a decode step is then a table lookup instead of two driver
+// calls per GEMM.
+struct TmapKey {
+  const void* base;
+  uint64_t cols, rows;
+  uint32_t box_cols, box_rows;
+  int dtype, swizzle, promo;
+  bool operator==(const TmapKey& o) const {
+    return base == o.base && cols == o.cols && rows == o.rows && box_cols == o.box_cols &&
+           box_rows == o.box_rows && dtype == o.dtype && swizzle == o.swizzle && promo == o.promo;
+  }
+};
+constexpr int kTmapSlots = 256;
+struct TmapEntry {
+  TmapKey key;
+  CUtensorMap map;
+  bool used;
+};
+static std::mutex g_tmap_mu;
+static TmapEntry g_tmap[kTmapSlots];
+
+static bool encode_2d_cached(CUtensorMap* map, CUtensorMapDataType dt, uint32_t esize, const void* base,
+                             uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+                             CUtensorMapSwizzle sw, CUtensorMapL2promotion promo, CUresult* res) {
+  const TmapKey key{base, cols, rows, box_cols, box_rows, static_cast<int>(dt), static_cast<int>(sw),
+                    static_cast<int>(promo)};
+  uint64_t h = reinterpret_cast<uintptr_t>(base) * 0x9E3779B97F4A7C15ull;
+  h ^= (cols * 31 + rows) * 0xC2B2AE3D27D4EB4Full;
+  h ^= (static_cast<uint64_t>(box_cols) << 32 | box_rows) + static_cast<uint64_t>(key.dtype * 7 + key.swizzle);
+  const int slot = static_cast<int>((h >> 32) % kTmapSlots);
+  {
+    std::lock_guard<std::mutex> lk(g_tmap_mu);
+    if (g_tmap[slot].used && g_tmap[slot].key == key) {
+      *map = g_tmap[slot].map;
+      *res = CUDA_SUCCESS;
+      return true;
+    }
+  }
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * esize};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  *res = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (*res != CUDA_SUCCESS) return false;
+  std::lock_guard<std::mutex> lk(g_tmap_mu);
+  g_tmap[slot] = TmapEntry{key, *map, true};
+  return true;
+}
+
 bool make_tmap_u32_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                       uint32_t box_cols, uint32_t box_rows, int swizzle_bytes) {
   if (!ensure_encode()) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 4};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
   CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
   if (swizzle_bytes == 32) sw = CU_TENSOR_MAP_SWIZZLE_32B;
   else if (swizzle_bytes == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
@@ -211,10 +261,9 @@ bool make_tmap_u32_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_
     set_error("make_tmap_u32_2d: unsupported swizzle span %d", swizzle_bytes);
     return false;
   }
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims,
-                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
+  CUresult r;
+  if (!encode_2d_cached(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, base, cols, rows, box_cols, box_rows, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, &r)) {
     set_error("cuTensorMapEncodeTiled(u32 %llux%llu box %ux%u) failed: %d", (unsigned long long)cols,
               (unsigned long long)rows, box_cols, box_rows, static_cast<int>(r));
     return false;
@@ -225,15 +274,9 @@ bool make_tmap_u32_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                        uint32_t box_cols, uint32_t box_rows) {
   if (!ensure_encode()) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
+  CUresult r;
+  if (!encode_2d_cached(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, box_cols, box_rows,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, &r)) {
     set_error("cuTensorMapEncodeTiled(bf16 %llux%llu box %ux%u) failed: %d", (unsigned long long)cols,
               (unsigned long long)rows, box_cols, box_rows, static_cast<int>(r));
     return false;
@@ -244,15 +287,9 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64
 bool make_tmap_bf16_2d_sw128(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                              uint32_t box_cols, uint32_t box_rows) {
   if (!ensure_encode()) return false;
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {box_cols, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
-                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
+  CUresult r;
+  if (!encode_2d_cached(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, box_cols, box_rows,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, &r)) {
     set_error("cuTensorMapEncodeTiled(bf16 %llux%llu box %ux%u) failed: %d", (unsigned long long)cols,
               (unsigned long long)rows, box_cols, box_rows, static_cast<int>(r));
     return false;
