@@ -107,6 +107,11 @@ size_t wna16_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits);
  *             concurrently must not share one workspace. May be NULL when the
  *             required size is 0, or when the kernel the call takes uses none;
  *             a call whose kernel uses one returns WQ_EINVAL without it.
+ *  Reproducibility: the CTA-pair decode and tensor-core kernels reduce in a
+ *  fixed order, so repeated calls give the same bits; the split-K streaming
+ *  kernels (WQ_ROUTE_DECODE_SPLITK, WQ_ROUTE_CHUNKED) add their partial sums
+ *  with fp32 atomics in arrival order, so their results may differ between
+ *  calls in the last bits (each within the documented accuracy).
  *  M >= 1, N >= 1, bits in 2..8. Shapes that the tensor-core kernel does not
  *  take (fewer than 65 tokens, see wq_debug_route) need K <= 16384 or, up to
  *  16 tokens, K a multiple of 1024 whose activations fit the decode kernels;
