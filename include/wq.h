@@ -112,10 +112,9 @@ size_t wna16_workspace_bytes(int64_t M, int64_t N, int64_t K, int bits);
  *  kernels (WQ_ROUTE_DECODE_SPLITK, WQ_ROUTE_CHUNKED) add their partial sums
  *  with fp32 atomics in arrival order, so their results may differ between
  *  calls in the last bits (each within the documented accuracy).
- *  M >= 1, N >= 1, bits in 2..8. Shapes that the tensor-core kernel does not
- *  take (fewer than 65 tokens, see wq_debug_route) need K <= 16384 or, up to
- *  16 tokens, K a multiple of 1024 whose activations fit the decode kernels;
- *  others return WQ_EUNSUPPORTED. */
+ *  M >= 1, N >= 1, bits in 2..8, K <= 1048576 below the tensor-core kernel's
+ *  token counts (fewer than 65 tokens, see wq_debug_route); larger K there
+ *  returns WQ_EUNSUPPORTED. */
 wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const wq_bf16* scales,
                      int64_t N, int64_t K, int bits, int group, wq_bf16* y,
                      void* workspace, size_t ws_bytes, void* stream);
@@ -130,7 +129,7 @@ wq_status wna16_gemm(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const
  *  Every other argument as wna16_gemm; workspace at least
  *  wna16_zp_workspace_bytes(). Same kernels as wna16_gemm, except that
  *  few-token shapes whose K half does not fit the CTA-pair decode kernel go
- *  to the chunked kernel (K <= 16384; larger K returns WQ_EUNSUPPORTED). */
+ *  to the chunked kernel. */
 wq_status wna16_gemm_zp(const wq_bf16* x, int64_t M, const uint32_t* Wpacked, const wq_bf16* scales,
                         const uint8_t* zeros, int64_t N, int64_t K, int bits, int group, wq_bf16* y,
                         void* workspace, size_t ws_bytes, void* stream);

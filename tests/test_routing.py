@@ -90,16 +90,19 @@ def test_bad_arguments(args):
         wq.debug_route(M, N, Kx, bits, sms, w4a8=w4a8)
 
 
-def test_shapes_no_kernel_takes():
-    """Below the tensor-core kernel's token counts the chunked kernel keeps a
-    CTA's scales in shared memory (K <= 16384); a shape that reaches it with a
-    larger K has no kernel, and the entry points refuse it
-    (WQ_EUNSUPPORTED) instead of failing at launch."""
-    assert wq.debug_route(24, 5120, 16384, 6, SMS) == "chunked"       # the largest K it takes
-    assert wq.debug_route(1, 5120, 16512, 6, SMS) == "none"           # not a multiple of 1024
-    assert wq.debug_route(24, 5120, 28672, 6, SMS) == "none"
-    assert wq.debug_route(64, 5120, 28672, 6, SMS) == "none"          # too few row tiles for the tensor cores
-    assert wq.debug_route(24, 5120, 28672, 4, SMS, w4a8=True) == "none"
+def test_long_k_below_the_tensor_core_token_counts():
+    """Below the tensor-core kernel's token counts the chunked kernel keeps at
+    most 128 groups of scales per CTA and splits a longer K over up to 64
+    CTAs (K <= 1048576); a longer K has no kernel, and the entry points refuse
+    it (WQ_EUNSUPPORTED) instead of failing at launch."""
+    assert wq.debug_route(24, 5120, 16384, 6, SMS) == "chunked"
+    assert wq.debug_route(1, 5120, 16512, 6, SMS) == "chunked"        # not a multiple of 1024
+    assert wq.debug_route(24, 5120, 28672, 6, SMS) == "chunked"
+    assert wq.debug_route(64, 5120, 28672, 6, SMS) == "chunked"       # too few row tiles for the tensor cores
+    assert wq.debug_route(24, 5120, 28672, 4, SMS, w4a8=True) == "chunked"
+    assert wq.debug_route(24, 5120, 1048576, 6, SMS) == "chunked"     # the largest K it takes
+    assert wq.debug_route(24, 5120, 1048576 + 128, 6, SMS) == "none"
+    assert wq.debug_route(1, 5120, 1048576 + 128, 6, SMS) == "none"
     assert wq.debug_route(64, 17408, 28672, 6, SMS) == "tensor_core"
     assert wq.debug_route(100, 5120, 28672, 6, SMS) == "tensor_core"
     assert wq.debug_route(16, 8192, 28672, 6, SMS) == "decode_splitk"
@@ -148,7 +151,7 @@ def test_zero_point_routes_and_workspace_query():
         if r == "chunked":
             assert need >= M * N * 4, (M, N, K, bits, sms)
         if r == "none":
-            assert K > 16384
+            assert K > 1048576
         sym = wq.debug_route(M, N, K, bits, sms)
         if sym == "tensor_core":
             assert r == "tensor_core"

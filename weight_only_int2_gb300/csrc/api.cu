@@ -113,7 +113,7 @@ wq_status check_workspace(const void* workspace, size_t ws_bytes, size_t need) {
 wq_status no_route(int64_t M, int64_t N, int64_t K) {
   return fail(WQ_EUNSUPPORTED,
               "no kernel takes M = %lld, N = %lld, K = %lld: below the tensor-core kernel's token counts "
-              "the streaming kernels take K <= 16384, or K a multiple of 1024 for up to 16 tokens",
+              "the streaming kernels take K <= 1048576",
               (long long)M, (long long)N, (long long)K);
 }
 

@@ -55,7 +55,8 @@ constexpr int kRowsPerWarp = 16;
 constexpr int kRowsPerCta = kWarps * kRowsPerWarp;  // 128
 constexpr int kStages = 4;
 constexpr int kXGroupsTimesNT = 16;     // x chunk: NT * XC == 16 groups of 8 tokens
-constexpr int kMaxGroupsPerCta = 128;   // K <= 16384 (scales of a CTA live in smem)
+constexpr int kMaxGroupsPerCta = 128;   // groups per CTA (its scales live in smem); K splits above
+constexpr int kMaxSplits = 64;          // K <= 64 * 128 * 128 = 1048576
 
 struct Params {
   const uint16_t* x;
@@ -340,20 +341,23 @@ struct Plan {
 };
 
 // Split-K choice: minimise (waves of resident CTAs) x (groups per CTA plus a
-// fixed per-CTA cost of about three groups).
+// fixed per-CTA cost of about three groups), with at most kMaxGroupsPerCta
+// groups per CTA (a longer K always splits).
 Plan make_plan(int64_t M, int64_t N, int64_t K, int sm_count) {
   Plan pl{};
   pl.nt = M <= 8 ? 1 : (M <= 16 ? 2 : (M <= 32 ? 4 : 8));
   pl.mchunks = static_cast<int>((M + pl.nt * 8 - 1) / (pl.nt * 8));
   pl.row_blocks = static_cast<int>((N + kRowsPerCta - 1) / kRowsPerCta);
   const int G = static_cast<int>(K / 128);
-  int best_gper = G;
+  const int min_splits = (G + kMaxGroupsPerCta - 1) / kMaxGroupsPerCta;
+  int best_gper = (G + min_splits - 1) / min_splits;
   if (M <= 64) {
     const int64_t base = static_cast<int64_t>(pl.row_blocks) * pl.mchunks;
     const int64_t resident = 2LL * sm_count;
     int64_t best_cost = -1;
-    for (int s = 1; s <= std::min(G, 64); ++s) {
+    for (int s = 1; s <= std::min(G, kMaxSplits); ++s) {
       const int gper = (G + s - 1) / s;
+      if (gper > kMaxGroupsPerCta) continue;
       const int splits = (G + gper - 1) / gper;
       const int64_t ctas = base * splits;
       const int64_t cost = ((ctas + resident - 1) / resident) * (gper + 3);
@@ -394,7 +398,7 @@ cudaError_t launch_nt(const Ctx& c, const CUtensorMap& tmap, const Params& prm, 
 
 }  // namespace
 
-bool gemv_supported(int64_t K) { return K / 128 <= kMaxGroupsPerCta; }
+bool gemv_supported(int64_t K) { return K / 128 <= static_cast<int64_t>(kMaxSplits) * kMaxGroupsPerCta; }
 
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   (void)K;
@@ -408,12 +412,16 @@ size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K) {
 }
 
 cudaError_t launch_gemv(const Ctx& c, const GemvArgs& a) {
-  if (a.K / 128 > kMaxGroupsPerCta) {
+  if (!gemv_supported(a.K)) {
     set_error("K = %lld exceeds the supported maximum of %d", static_cast<long long>(a.K),
-              kMaxGroupsPerCta * 128);
+              kMaxSplits * kMaxGroupsPerCta * 128);
     return cudaErrorInvalidValue;
   }
   const Plan pl = make_plan(a.M, a.N, a.K, c.sm_count);
+  if (pl.gper > kMaxGroupsPerCta) {
+    set_error("chunked plan: %d groups per CTA exceed %d", pl.gper, kMaxGroupsPerCta);
+    return cudaErrorInvalidValue;
+  }
   CUtensorMap tmap;
   const uint64_t words = static_cast<uint64_t>(a.K) * a.bits / 32;
   if (!make_tmap_u32_2d(&tmap, a.packed, words, static_cast<uint64_t>(a.N), 4u * a.bits, kRowsPerWarp))

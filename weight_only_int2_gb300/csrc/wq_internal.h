@@ -100,8 +100,9 @@ struct GemvArgs {
 
 // Workspace bytes the weight-streaming GEMM needs for this shape.
 size_t gemv_workspace_bytes(int64_t M, int64_t N, int64_t K);
-// Whether the chunked kernel takes K: a CTA keeps the scales of all its
-// groups in shared memory, at most 128 groups (K <= 16384).
+// Whether the chunked kernel takes K: a CTA keeps the scales of its groups in
+// shared memory, at most 128 groups, and a longer K splits over up to 64
+// CTAs (K <= 1048576).
 bool gemv_supported(int64_t K);
 
 cudaError_t launch_gemv(const Ctx& c, const GemvArgs& a);
@@ -179,7 +180,7 @@ inline Route route_wna16(int64_t M, int64_t N, int64_t K, int bits, int sm_count
 
 // Asymmetric groups (a zero point per row and group): the kernels of
 // route_wna16 but the persistent split-K decode kernel, which has no
-// zero-point mode; the chunked kernel takes those shapes (K <= 16384).
+// zero-point mode; the chunked kernel takes those shapes.
 inline Route route_wna16_zp(int64_t M, int64_t N, int64_t K, int bits, int sm_count) {
   if (use_prefill(M, N, K, bits, sm_count)) return Route::kTensorCore;
   if (decode2_supported(M, N, K, bits, sm_count, true)) return Route::kDecodePair;
