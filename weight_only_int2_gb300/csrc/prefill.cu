@@ -56,20 +56,23 @@ constexpr int kTmemCols = 512;
 // together (measured: 0.79 of the bf16 peak at M = 8192 against 0.71 per
 // stage; four stages per commit starve the A ring at 0.54).
 constexpr int kSPC = 2;
-constexpr int kMaxNX = 6;    // activation stages in shared memory (upper bound)
-constexpr int kMaxNP = 4;    // packed-weight slots, one group each (upper bound)
+constexpr int kMaxNX = 8;    // activation stages in shared memory (upper bound, at most kNA)
+constexpr int kMaxNP = 12;   // packed-weight slots, one group each (upper bound)
 constexpr int kTeamWarps = 4;                  // one team: 128 rows x 64 codes
 constexpr int kTeams = 4;                      // team j takes stages j (mod 4)
 constexpr int kDeqWarps = kTeams * kTeamWarps;
 constexpr int kThreads = (3 + kDeqWarps) * 32;  // 608
 static_assert(kNA % kTeams == 0, "each team must own whole A slots");
 
-// Shared memory: activation stages (3..6) and packed-weight slots (2 or 4).
-// Preference: 4 packed slots with at least 5 activation stages, else the
-// deepest activation ring with 2 slots. The slot count is even: a slot's
-// previous group then has the same parity, so the teams that wait on it have
-// consumed that previous phase (a parity wait is only sound when the phase
-// before the awaited one has completed).
+// Shared memory: activation stages (3..8) and packed-weight slots (2..12).
+// Preference: at least 5 activation stages beside 4 packed slots, else the
+// deepest activation ring with 2 slots; then as many packed slots as the rest
+// of shared memory holds. Few tokens per tile (TN = 128) leave room for 8 to
+// 12 groups of weights in flight, which is what a tile that is bound by the
+// weight stream needs. The slot count is even: a slot's previous group then
+// has the same parity, so the teams that wait on it have consumed that
+// previous phase (a parity wait is only sound when the phase before the
+// awaited one has completed).
 template <int B, int TN>
 struct Layout {
   static constexpr int kXStage = TN * kBK * 2;
@@ -78,14 +81,23 @@ struct Layout {
   static constexpr bool fits(int nx, int np) { return nx * kXStage + np * kPSlot <= kBudget; }
   static constexpr int pick_nx() {
     for (int nx = kMaxNX; nx >= 5; --nx)
-      if (fits(nx, kMaxNP)) return nx;
+      if (fits(nx, 4)) return nx;
     for (int nx = kMaxNX; nx >= 3; --nx)
       if (fits(nx, 2)) return nx;
     return 0;
   }
   static constexpr int kNX = pick_nx();
-  static constexpr int kNP = fits(kNX, kMaxNP) ? kMaxNP : 2;
-  static_assert(kNX >= 3 && fits(kNX, kNP), "prefill rings do not fit shared memory");
+  static constexpr int pick_np() {
+    for (int np = kMaxNP; np >= 2; np -= 2)
+      if (fits(kNX, np)) return np;
+    return 0;
+  }
+  static constexpr int kNP = pick_np();
+  // the activation producer refills a slot once the MMAs of the stage kNX
+  // back have completed; that also proves the "full" phase kNA stages back
+  // complete only while kNX <= kNA
+  static_assert(kNX <= kNA, "activation ring deeper than the A ring");
+  static_assert(kNX >= 3 && kNP >= 2 && kNP % 2 == 0 && fits(kNX, kNP), "prefill rings do not fit shared memory");
   static constexpr int kXOff = 0;
   static constexpr int kPOff = kNX * kXStage;
   static constexpr int kBytes = kPOff + kNP * kPSlot;
