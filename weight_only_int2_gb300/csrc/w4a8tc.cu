@@ -16,11 +16,17 @@
 // accumulator; the scale is applied in fp32 when the group is read out.
 //
 // Persistent kernel, one CTA per SM; a tile is 128 weight rows (MMA M) x TN
-// = 128 tokens (MMA N). Tensor memory (512 columns): two group accumulators
-// of TN columns (group g in buffer g % 2, so the MMAs of one group overlap
-// the read-out of the other) and a ring of kNA = (512 - 2 TN) / 32 = 8
-// stages of the A operand (64 codes each).
-// Warp roles:
+// tokens (MMA N): 160, or 128 where 160 would pad the tokens more. Tensor
+// memory (512 columns): two group accumulators of TN columns (group g in
+// buffer g % 2, so the MMAs of one group overlap the read-out of the other)
+// and a ring of kNA = (512 - 2 TN) / 32 stages of the A operand, 64 codes
+// each (8 stages at TN = 128, 6 at TN = 160).
+// Warp roles (24 warps in six warpgroups). Reading a group out and writing
+// the A operand are done by different warps, so that neither waits for the
+// other: an accumulator is freed as soon as its MMAs end, and the A operand
+// of the next groups is written while they run. The read-out warpgroups take
+// 96 registers a thread (setmaxnreg) from the two others, which keep 48, so
+// that every read-out load of a group is in flight at once.
 //   warp 0      TMA producer for the activation codes [TN x 64] (bf16,
 //               128-byte swizzle, zero fill past M) of each stage.
 //   warp 1      allocates tensor memory; one thread issues, per group, the
@@ -29,16 +35,16 @@
 //               accumulator is complete and its slots are free).
 //   warp 2      TMA producer for the packed 4-bit weights, one group
 //               [128 rows x 64 bytes] per load.
-//   warps 3-18  four teams of 4 warps. Team j writes the A operand of the
-//               stages j (mod 4): a thread turns the 64 codes of one weight
-//               row into q - 8 and stores them to its TMEM lane. Every one of
-//               the 16 warps reads out every group: warp (j, quarter) takes
-//               TN / 4 token columns of its 32 rows, frees the accumulator,
-//               and adds s[n, g] * acc into fp32 running sums; after the last
-//               group of a tile it stores bf16(sx[m] * sum). A warp reads a
-//               group out as soon as its MMAs end, then writes the A operand
-//               of the group kNA / 2 ahead into the slots they freed, so the
-//               tensor core always has the next groups queued.
+//   warp 3      idle (completes the first warpgroup).
+//   warps 4-7   the A operand: a thread turns the 128 codes of one weight row
+//               of a group into q - 8 and stores them to its TMEM lane (the
+//               group's two stages), once the MMAs that read those slots
+//               before have ended.
+//   warps 8-23  read-out: warp (set c, quarter) takes token columns
+//               c TN / 4 .. + TN / 4 - 1 of its 32 rows of every group (all
+//               its loads in flight at once, one wait), frees the
+//               accumulator and adds s[n, g] * acc into fp32 running sums;
+//               after the last group of a tile it stores bf16(sx[m] * sum).
 // kAcc: write the exact accumulators acc[m, n, g] as int32 instead of y (the
 // test and debug mode of the same kernel).
 // All mbarrier waits are bounded; a timeout records WQ_ETIMEOUT and every
@@ -58,33 +64,42 @@ constexpr int kNB = 8;          // stage barriers (full), indexed by stage mod 8
 constexpr int kNG = 8;          // group barriers (gdone), indexed by group mod 8
 constexpr int kTmemCols = 512;
 constexpr int kMaxNX = 8;       // activation stages in shared memory (<= kNB)
-constexpr int kNP = 4;          // packed-weight slots, one group each (even)
-constexpr int kTeamWarps = 4;   // one team: 128 rows x 64 codes
-constexpr int kTeams = 4;       // team j takes stages j (mod 4)
-constexpr int kDeqWarps = kTeams * kTeamWarps;
-constexpr int kThreads = (3 + kDeqWarps) * 32;  // 608
-constexpr int kPSlot = kBM * 64;                // one group of 128 rows of 4-bit codes
-// Tokens per tile (MMA N). 128 leaves room for an 8-stage A ring beside the
-// two accumulators and keeps the running sums (32 per thread) in registers;
-// 192 (a 4-stage ring, 48 sums) measured slower at every token count from
-// 512 to 8192, its running sums spilling at the register limit of 19 warps.
-constexpr int kTN = 128;
+constexpr int kMaxNP = 8;       // packed-weight slots, one group each (even)
+constexpr int kAWarps = 4;      // the A operand: one warp per TMEM lane quarter
+constexpr int kRWarps = 16;     // read-out: 4 column sets x 4 lane quarters
+constexpr int kAWarp0 = 4;
+constexpr int kRWarp0 = kAWarp0 + kAWarps;
+constexpr int kThreads = (kRWarp0 + kRWarps) * 32;  // 768: 80 registers a thread at launch
+// setmaxnreg split of the 768 x 80 registers the block is launched with:
+// warpgroups 0 and 1 (producers, MMA, A operand) give 32 each of theirs to
+// the four read-out warpgroups: 256 x 48 + 512 x 96 = 768 x 80.
+constexpr int kRegsLow = 48, kRegsHigh = 96;
+static_assert(256 * kRegsLow + 512 * kRegsHigh <= kThreads * 80, "register split above the launch's registers");
+constexpr int kPSlot = kBM * 64;                    // one group of 128 rows of 4-bit codes
 
 template <int TN>
 struct WLayout {
   static constexpr int kNA = (kTmemCols - 2 * TN) / 32;  // A stages in tensor memory
   static constexpr int kACol = 2 * TN;                    // A ring: columns [2 TN, 512)
-  static constexpr int kLead = kNA / 2;                   // groups of A a warp writes ahead
-  static_assert(kNA >= 4 && kNA % kTeams == 0 && kNA <= kNB, "A ring must give each team whole slots");
+  static_assert(kNA >= 4 && kNA % 2 == 0 && kNA <= kNB, "A ring must hold whole groups");
+  static constexpr int kCols = TN / 4;  // token columns of one read-out warp
+  static_assert(kCols % 8 == 0, "read-out in loads of eight columns");
   static constexpr int kXStage = TN * kBK * 2;
   static constexpr int kBudget = 227 * 1024 - 1024 - 512;  // minus alignment slack and static smem
+  static constexpr bool fits(int nx, int np) { return nx * kXStage + np * kPSlot <= kBudget; }
   static constexpr int pick_nx() {
     for (int nx = kMaxNX; nx >= 3; --nx)
-      if (nx * kXStage + kNP * kPSlot <= kBudget) return nx;
+      if (fits(nx, 4)) return nx;
     return 0;
   }
   static constexpr int kNX = pick_nx();
-  static_assert(kNX >= 3, "W4A8 rings do not fit shared memory");
+  static constexpr int pick_np() {
+    for (int np = kMaxNP; np >= 2; np -= 2)
+      if (fits(kNX, np)) return np;
+    return 0;
+  }
+  static constexpr int kNP = pick_np();
+  static_assert(kNX >= 3 && kNP >= 4 && kNP % 2 == 0, "W4A8 rings do not fit shared memory");
   static constexpr int kPOff = kNX * kXStage;
   static constexpr size_t kSmem = static_cast<size_t>(kPOff + kNP * kPSlot) + 1024;  // + alignment slack
 };
@@ -123,18 +138,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     w4a8_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                    const WParams p) {
   using L = WLayout<TN>;
-  constexpr int NX = L::kNX, NA = L::kNA;
-  constexpr int kCols = TN / kTeams;  // token columns a warp reads out
+  constexpr int NX = L::kNX, NA = L::kNA, NP = L::kNP, kCols = L::kCols;
   extern __shared__ uint8_t smem_raw[];
   // full[j]: stage (j mod kNB) has its activation bytes and its A operand
-  //          (arrivals: the activation producer's expect-tx + one team);
+  //          (arrivals: the activation producer's expect-tx + the A warps);
   // gdone[g]: the MMAs of group (g mod kNG) completed (one commit per group,
   //          after both its stages): the group's accumulator is complete, its
   //          two A slots are free and, NX stages later in the sequence, its
   //          activation slots;
   // pfull/pempty: packed-weight slots;
   // acce[b]: group accumulator b read out.
-  __shared__ __align__(8) uint64_t full[kNB], gdone[kNG], pfull[kNP], pempty[kNP], acce[2];
+  __shared__ __align__(8) uint64_t full[kNB], gdone[kNG], pfull[kMaxNP], pempty[kMaxNP], acce[2];
   // the group barrier that releases stage j of the sequence, and its phase
   auto gbar = [&](uint32_t j) -> uint64_t* { return &gdone[(j >> 1) % kNG]; };
   auto gphase = [](uint32_t j) -> uint32_t { return ((j >> 1) / kNG) & 1u; };
@@ -157,13 +171,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t total_groups = static_cast<uint32_t>(my_tiles) * static_cast<uint32_t>(G);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNB; ++s) mbar_init(&full[s], kTeamWarps + 1);
+    for (int s = 0; s < kNB; ++s) mbar_init(&full[s], kAWarps + 1);
     for (int s = 0; s < kNG; ++s) mbar_init(&gdone[s], 1);
-    for (int s = 0; s < kNP; ++s) {
+    for (int s = 0; s < NP; ++s) {
       mbar_init(&pfull[s], 1);
-      mbar_init(&pempty[s], 2 * kTeamWarps);  // the two teams that share a group
+      mbar_init(&pempty[s], kAWarps);
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&acce[b], kDeqWarps);
+    for (int b = 0; b < 2; ++b) mbar_init(&acce[b], kRWarps);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -178,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
+  if (warp < kAWarp0) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
   if (warp == 0) {
     // ---- activation codes: stage i of a tile covers k = 64 i .. 64 i + 63;
     // slot it % NX is free once stage it - NX is done (NX <= kNB: the done
@@ -203,14 +218,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 2) {
-    // ---- packed weights: group gi into slot gi % kNP
+    // ---- packed weights: group gi into slot gi % NP
     if (lane == 0) {
       uint32_t gi = 0;
       for (int t = first; t < ntiles && !s_abort; t += step) {
         const int n0 = (t % p.row_tiles) * kBM;
         for (int g = 0; g < G; ++g, ++gi) {
-          const uint32_t sl = gi % kNP;
-          if (gi >= static_cast<uint32_t>(kNP) && !mbar_wait_backoff<256>(&pempty[sl], ((gi / kNP) - 1) & 1)) {
+          const uint32_t sl = gi % NP;
+          if (gi >= static_cast<uint32_t>(NP) && !mbar_wait_backoff<256>(&pempty[sl], ((gi / NP) - 1) & 1)) {
             record_status(p.status, kStatusTimeout);
             s_abort = 1;
             break;
@@ -258,73 +273,78 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
-    // ---- A operand + read-out (warps 3..18). Warp w owns TMEM lane quarter
-    // q = w % 4 (rows 32 q .. 32 q + 31 of the tile); team j = (w - 3) / 4
-    // writes the A operand of stages it = j (mod 4) (groups of parity j / 2,
-    // half j % 2) and reads token columns j * kCols .. + kCols - 1 out of
-    // every group's accumulator.
-    const int dw = warp - 3;
-    const int team = dw / kTeamWarps;
+  } else if (warp == 3) {
+    // idle
+  } else if (warp < kRWarp0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    // ---- A operand (warps 4..7). Warp w owns TMEM lane quarter q = w % 4
+    // (rows 32 q .. 32 q + 31 of the tile) and writes stages 2 gi, 2 gi + 1
+    // of every group gi into slots (2 gi) % NA, (2 gi + 1) % NA, once the
+    // MMAs of the group NA / 2 before (the slots' previous group) have
+    // completed.
     const int q = warp & 3;
-    const int h = team & 1, gpar = team >> 1;
     const int r = 32 * q + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-
-    // writes the A operand of group gi (this team's half); warp-uniform,
-    // false on timeout
-    auto write_a = [&](uint32_t gi) -> bool {
-      const uint32_t it = 2 * gi + h, a = it % NA, pslot = gi % kNP;
+    for (uint32_t gi = 0; gi < total_groups; ++gi) {
+      const uint32_t it = 2 * gi, pslot = gi % NP;
       bool go = !s_abort;
-      if (go) go = mbar_wait_backoff<32>(&pfull[pslot], (gi / kNP) & 1);
-      if (go && it >= static_cast<uint32_t>(NA)) go = mbar_wait_backoff<32>(gbar(it - NA), gphase(it - NA));
+      if (go) go = mbar_wait_bounded(&pfull[pslot], (gi / NP) & 1);
+      if (go && it >= static_cast<uint32_t>(NA)) go = mbar_wait_bounded(gbar(it - NA), gphase(it - NA));
       if (!__all_sync(0xFFFFFFFFu, go)) {
         if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
         s_abort = 1;
-        return false;
+        break;
       }
-      // half h of row r: 16-byte chunks 2h, 2h + 1 of the 64-byte row,
-      // loaded with the TMA 64-byte swizzle (chunk c sits at c ^ ((r >> 1) & 3))
+      // row r: the four 16-byte chunks of the 64-byte row, loaded with the
+      // TMA 64-byte swizzle (chunk c sits at c ^ ((r >> 1) & 3))
       const uint8_t* prow = ps + pslot * kPSlot + r * 64;
+      uint4 v[4];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int c = 2 * h + half;
-        const uint4 v = *reinterpret_cast<const uint4*>(prow + ((c ^ packed_xor<4>(r)) << 4));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(prow + ((c ^ packed_xor<4>(r)) << 4));
+      // the slot may be refilled once every lane's reads are done: the refill
+      // is a TMA (async-proxy) write, which these generic-proxy reads are
+      // ordered before only by a proxy fence in each reading thread
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pempty[pslot]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        // chunk c: codes 32 c .. 32 c + 31 = half c % 2 of stage it + c / 2
+        const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
         uint32_t o[16];
         exact_slice4(w, o);
-        tmem_st16(tmem + lane_base + L::kACol + a * (kBK / 2) + 16 * half, o);
+        tmem_st16(tmem + lane_base + L::kACol + ((it + c / 2) % NA) * (kBK / 2) + 16 * (c & 1), o);
       }
       tmem_wait_st();
-      tc_fence_before();  // the A tile before the arrival the MMA waits on
+      tc_fence_before();  // the A tiles before the arrivals the MMA waits on
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&full[it % kNB]);
-        mbar_arrive(&pempty[pslot]);
+        mbar_arrive(&full[(it + 1) % kNB]);
       }
-      return true;
-    };
-
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+    // ---- read-out (warps 8..23). Warp w owns TMEM lane quarter q = w % 4
+    // (rows 32 q .. 32 q + 31) and token columns c kCols .. + kCols - 1,
+    // c = (w - 8) / 4, of every group's accumulator.
+    const int cset = (warp - kRWarp0) / 4;
+    const int q = warp & 3;
+    const int r = 32 * q + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
     float run[kCols];
 #pragma unroll
     for (int j = 0; j < kCols; ++j) run[j] = 0.0f;
-
-    bool failed = false;  // a wait of this warp gave up (warp-uniform)
-    // the A operand of the first kLead groups
-    for (uint32_t gi = 0; gi < static_cast<uint32_t>(L::kLead) && gi < total_groups; ++gi)
-      if (static_cast<int>(gi & 1) == gpar && !failed && !write_a(gi)) failed = true;
     // group gi of the sequence is group g of tile t; the row, the token
     // columns and the scale row change once per tile (no division per group)
     int t = first, g = 0;
     int64_t n = static_cast<int64_t>(t % p.row_tiles) * kBM + r;
-    int64_t m0 = static_cast<int64_t>(t / p.row_tiles) * TN + team * kCols;
+    int64_t m0 = static_cast<int64_t>(t / p.row_tiles) * TN + cset * kCols;
     // the scale s[n, g] of the group read out next, loaded one group ahead
-    float s_next = (!kAcc && n < p.N) ? bf16_bits_to_float(p.scales[n * G]) : 0.0f;
+    float s_next = (!kAcc && my_tiles > 0 && n < p.N) ? bf16_bits_to_float(p.scales[n * G]) : 0.0f;
     for (uint32_t gi = 0; gi < total_groups; ++gi) {
-      // 1. read out group gi: the MMAs of group gi + 2 wait for this buffer,
-      //    so it comes first; the A operand is needed one group later
       const uint32_t b = gi & 1u;
-      if (failed || !__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_backoff<32>(&gdone[gi % kNG], (gi / kNG) & 1))) {
+      if (!__all_sync(0xFFFFFFFFu, !s_abort && mbar_wait_bounded(&gdone[gi % kNG], (gi / kNG) & 1))) {
         if (lane == 0 && !s_abort) record_status(p.status, kStatusTimeout);
         s_abort = 1;
         break;
@@ -339,47 +359,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_next = n2 < p.N ? bf16_bits_to_float(p.scales[n2 * G]) : 0.0f;
         }
       }
-      const uint32_t col0 = tmem + lane_base + b * TN + team * kCols;
-      // consumes 16 columns of the group: running sums, or (kAcc) the
-      // integer accumulators themselves
-      auto use16 = [&](int c, const uint32_t (&v)[16]) {
-        if constexpr (kAcc) {
-          if (n < p.N) {
+      const uint32_t col0 = tmem + lane_base + b * TN + cset * kCols;
+      // every load of the warp's columns in flight, one wait, then free the
+      // buffer and use the values
+      uint32_t v[kCols];
+      tmem_ld_cols<kCols>(col0, v);
+      tmem_wait_ld_all<kCols>(v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[b]);
+      if constexpr (kAcc) {
+        if (n < p.N) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int64_t m = m0 + 16 * c + j;
-              if (m < p.M) p.acc[(m * p.N + n) * G + g] = __float2int_rn(__uint_as_float(v[j]));
-            }
+          for (int j = 0; j < kCols; ++j) {
+            const int64_t m = m0 + j;
+            if (m < p.M) p.acc[(m * p.N + n) * G + g] = __float2int_rn(__uint_as_float(v[j]));
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) run[16 * c + j] = fmaf(sc, __uint_as_float(v[j]), run[16 * c + j]);
         }
-      };
-      auto release = [&]() {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce[b]);
-      };
-      if constexpr (kCols <= 32) {
-        // every load in flight at once, one wait, then free the buffer
-        uint32_t v[kCols / 16][16];
-#pragma unroll
-        for (int c = 0; c < kCols / 16; ++c) tmem_ld16_nowait(col0 + 16 * c, v[c]);
-        tmem_wait_ld();
-        release();
-#pragma unroll
-        for (int c = 0; c < kCols / 16; ++c) use16(c, v[c]);
       } else {
-        // 16 columns at a time (registers: the running sums stay resident)
 #pragma unroll
-        for (int c = 0; c < kCols / 16; ++c) {
-          uint32_t v[16];
-          tmem_ld16_nowait(col0 + 16 * c, v);
-          tmem_wait_ld();
-          if (c == kCols / 16 - 1) release();
-          use16(c, v);
-        }
+        for (int j = 0; j < kCols; ++j) run[j] = fmaf(sc, __uint_as_float(v[j]), run[j]);
       }
       if constexpr (!kAcc) {
         if (g == G - 1) {
@@ -407,12 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         g = 0;
         t += step;
         n = static_cast<int64_t>(t % p.row_tiles) * kBM + r;
-        m0 = static_cast<int64_t>(t / p.row_tiles) * TN + team * kCols;
+        m0 = static_cast<int64_t>(t / p.row_tiles) * TN + cset * kCols;
       }
-      // 2. the A operand kLead groups ahead (its slot was freed by the MMAs
-      //    of group gi, which have completed)
-      const uint32_t ga = gi + L::kLead;
-      if (ga < total_groups && static_cast<int>(ga & 1) == gpar && !failed && !write_a(ga)) failed = true;
     }
   }
 
@@ -442,18 +437,31 @@ cudaError_t wlaunch(const Ctx& c, const CUtensorMap& xmap, const CUtensorMap& wm
   return cudaGetLastError();
 }
 
+template <int TN>
+cudaError_t launch_tn(const Ctx& c, const uint16_t* xqb, const uint32_t* packed4, const WParams& prm) {
+  CUtensorMap xmap, wmap;
+  if (!make_tmap_bf16_2d_sw128(&xmap, xqb, static_cast<uint64_t>(prm.K), static_cast<uint64_t>(prm.M), kBK, TN))
+    return cudaErrorInvalidValue;
+  // 4-bit rows of a group are 64 bytes: loaded with the 64-byte swizzle so
+  // that the rows of a tile spread over the shared-memory banks
+  if (!make_tmap_u32_2d(&wmap, packed4, static_cast<uint64_t>(prm.K) / 8, static_cast<uint64_t>(prm.N), 16u, kBM,
+                        64))
+    return cudaErrorInvalidValue;
+  return prm.acc != nullptr ? wlaunch<TN, true>(c, xmap, wmap, prm) : wlaunch<TN, false>(c, xmap, wmap, prm);
+}
+
 }  // namespace
+
+// Tokens per tile: 160 (less A-operand work per token) unless its last tile
+// would pad the tokens by more than a few per cent beyond 128-token tiles.
+int w4a8_tile_tokens(int64_t M) {
+  const int64_t p128 = (M + 127) / 128 * 128, p160 = (M + 159) / 160 * 160;
+  return p160 * 100 <= p128 * 104 ? 160 : 128;
+}
 
 cudaError_t launch_w4a8_tc(const Ctx& c, const uint16_t* xqb, const float* sx, const uint32_t* packed4,
                            const uint16_t* scales, int64_t M, int64_t N, int64_t K, uint16_t* y, int32_t* acc) {
   if (M < 1 || N < 1 || K < 128 || K % 128 != 0) return cudaErrorInvalidValue;
-  CUtensorMap xmap, wmap;
-  if (!make_tmap_bf16_2d_sw128(&xmap, xqb, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBK, kTN))
-    return cudaErrorInvalidValue;
-  // 4-bit rows of a group are 64 bytes: loaded with the 64-byte swizzle so
-  // that the rows of a tile spread over the shared-memory banks
-  if (!make_tmap_u32_2d(&wmap, packed4, static_cast<uint64_t>(K) / 8, static_cast<uint64_t>(N), 16u, kBM, 64))
-    return cudaErrorInvalidValue;
   WParams prm{};
   prm.scales = scales;
   prm.M = M;
@@ -464,7 +472,7 @@ cudaError_t launch_w4a8_tc(const Ctx& c, const uint16_t* xqb, const float* sx, c
   prm.sx = sx;
   prm.acc = acc;
   prm.status = c.status;
-  return acc != nullptr ? wlaunch<kTN, true>(c, xmap, wmap, prm) : wlaunch<kTN, false>(c, xmap, wmap, prm);
+  return w4a8_tile_tokens(M) == 160 ? launch_tn<160>(c, xqb, packed4, prm) : launch_tn<128>(c, xqb, packed4, prm);
 }
 
 }  // namespace wq

@@ -93,6 +93,31 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[1
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
+// N (a multiple of 8) consecutive 32-bit columns of 32 lanes, as loads of
+// 8 columns, all in flight; completes with tmem_wait_ld_all.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N % 8 == 0, "columns in loads of 8");
+#pragma unroll
+  for (int c = 0; c < N / 8; ++c) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[8 * c]), "=r"(r[8 * c + 1]), "=r"(r[8 * c + 2]), "=r"(r[8 * c + 3]), "=r"(r[8 * c + 4]),
+                   "=r"(r[8 * c + 5]), "=r"(r[8 * c + 6]), "=r"(r[8 * c + 7])
+                 : "r"(taddr + 8 * c));
+  }
+}
+// tcgen05.wait::ld for the registers of tmem_ld_cols: each group of eight is
+// named by an empty statement after the wait, so that no use of them can be
+// moved above it.
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld_all(uint32_t (&r)[N]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int c = 0; c < N / 8; ++c)
+    asm volatile(""
+                 : "+r"(r[8 * c]), "+r"(r[8 * c + 1]), "+r"(r[8 * c + 2]), "+r"(r[8 * c + 3]), "+r"(r[8 * c + 4]),
+                   "+r"(r[8 * c + 5]), "+r"(r[8 * c + 6]), "+r"(r[8 * c + 7]));
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Thread t of the warp writes 16 consecutive 32-bit columns of TMEM lane
