@@ -450,14 +450,14 @@ cudaError_t launch_tn(const Ctx& c, const uint16_t* xqb, const uint32_t* packed4
   return prm.acc != nullptr ? wlaunch<TN, true>(c, xmap, wmap, prm) : wlaunch<TN, false>(c, xmap, wmap, prm);
 }
 
-}  // namespace
-
 // Tokens per tile: 160 (less A-operand work per token) unless its last tile
 // would pad the tokens by more than a few per cent beyond 128-token tiles.
 int w4a8_tile_tokens(int64_t M) {
   const int64_t p128 = (M + 127) / 128 * 128, p160 = (M + 159) / 160 * 160;
   return p160 * 100 <= p128 * 104 ? 160 : 128;
 }
+
+}  // namespace
 
 cudaError_t launch_w4a8_tc(const Ctx& c, const uint16_t* xqb, const float* sx, const uint32_t* packed4,
                            const uint16_t* scales, int64_t M, int64_t N, int64_t K, uint16_t* y, int32_t* acc) {
