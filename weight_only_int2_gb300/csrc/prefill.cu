@@ -17,7 +17,7 @@
 // Tensor memory (512 columns): the fp32 accumulator in columns 0..TN-1 and a
 // ring of 8 dequantized A stages (32 columns each) in columns 256..511, so
 // the weights never pass through shared memory once dequantized; shared
-// memory holds up to 6 activation stages and 2-4 packed-weight groups.
+// memory holds up to 8 activation stages and 2-12 packed-weight groups.
 // Warp roles:
 //   warp 0      TMA producer for the activation tile [TN x 64] (128-byte
 //               swizzle, zero fill past M) of each stage.
